@@ -1,0 +1,176 @@
+/*
+ * bdattn -- per-document causal (block-diagonal) attention for one
+ * context-parallel query shard, forward and backward, on GB300 (sm_103a).
+ *
+ * What is computed (NVIDIA NeMo AutoModel API pages):
+ *  - blockdiag_cp.kernels, `_cp_blockdiag_mask`: a local query row at global
+ *    position p may attend key position s iff both carry the same document id,
+ *    neither is padding (id 0), and s <= p; the diagonal is always allowed.
+ *  - gemma4_moe.cp_local_ring (module text): the sliding layer adds a left
+ *    window on top of bottom-right causal; here a window W > 0 also requires
+ *    p - s < W.
+ *  - blockdiag_cp.kernels, `_cp_blockdiag_varlen`: the result equals mask +
+ *    softmax attention on real query rows; padding is a contiguous tail so the
+ *    real local rows are a prefix; padding query rows are returned as zeros.
+ *    One varlen segment per document the local rows touch: q segment = the
+ *    local rows of that document, k segment = [doc_start, last_local_q + 1).
+ *  - blockdiag_cp.kernels, `precompute_blockdiag_varlen_meta`: the
+ *    segmentation is built once per step, with no host synchronisation.
+ *
+ * Geometry of a virtual context-parallel rank r of cp_size ranks:
+ *   local query rows are global positions [row_offset, row_offset + L)
+ *   (row_offset = r * L); the K/V buffer holds global positions
+ *   [kv_offset, kv_offset + S_kv) and must contain [s_first, real_end) of
+ *   every batch row (the left-halo plan's needed range, blockdiag_cp.exchange).
+ *
+ * Layouts (all contiguous, row-major):
+ *   doc_ids  int32 [B, S_full]        0 = padding, > 0 = document id
+ *   q, dout  bf16  [B, Hq,  L,    D]
+ *   k, v     bf16  [B, Hkv, S_kv, D]  query head h reads kv head h / (Hq/Hkv)
+ *   out      bf16  [B, Hq,  L,    D]
+ *   lse      fp32  [B, Hq,  L]        natural-log sum-exp; -inf on padding rows
+ *   dq       fp32 or bf16 [B, Hq, L, D]
+ *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group
+ * D must be 64, 128 or 256. All device pointers are caller-owned and must be
+ * 16-byte aligned. The library allocates no device memory and never
+ * synchronises the stream; every entry point only enqueues work on `stream`.
+ *
+ * Errors:
+ *   - return value: BD_OK, or an argument / CUDA error found on the host
+ *     before or at launch (nothing, or nothing further, is enqueued);
+ *   - *status (one device int32, zero it before the first call of a step):
+ *     kernels OR BD_STATUS_* bits into it. When a bit is set, later kernels
+ *     skip their work (their outputs are left unwritten) instead of faulting.
+ */
+#ifndef BDATTN_H
+#define BDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef void* bd_stream_t;
+
+typedef struct {
+  int B;          /* batch rows */
+  int Hq;         /* query heads */
+  int Hkv;        /* key/value heads; Hq % Hkv == 0 */
+  int D;          /* head dim: 64, 128 or 256 */
+  int S_full;     /* length of each doc_ids row (full padded sequence) */
+  int L;          /* local query rows */
+  int row_offset; /* global position of local row 0 */
+  int kv_offset;  /* global position of K/V buffer row 0 */
+  int S_kv;       /* K/V buffer rows */
+  int window;     /* left window W (> 0: also require p - s < W); <= 0: none */
+  float scale;    /* softmax scale; <= 0 means D^-0.5 */
+} bd_geom;
+
+/* Host return codes. */
+#define BD_OK 0
+#define BD_ERR_ARG 1         /* invalid argument; nothing enqueued */
+#define BD_ERR_CUDA 2        /* a CUDA runtime/driver call failed */
+#define BD_ERR_UNSUPPORTED 3 /* device is not a Blackwell sm_10x part */
+
+/* Device status bits (OR-ed into *status). */
+#define BD_STATUS_LAYOUT 0x1   /* a doc id < 0, a document after padding, or a
+                                  local document id that also occurs before its
+                                  own run (ids must form one contiguous run) */
+#define BD_STATUS_KV_RANGE 0x2 /* K/V buffer misses part of [need_lo, real_end) */
+#define BD_STATUS_BOUNDS 0x4   /* segment table inconsistent with the geometry */
+#define BD_STATUS_TIMEOUT 0x8  /* a pipeline wait exceeded its time limit */
+
+/* Gradient output dtypes for bd_attn_bwd. */
+#define BD_DTYPE_F32 0
+#define BD_DTYPE_BF16 1
+
+/* Segment-table field indices within each batch row's header (int32). */
+#define BD_SEG_N_REAL 0
+#define BD_SEG_N_SEG 1
+#define BD_SEG_S_FIRST 2
+#define BD_SEG_REAL_END 3
+#define BD_SEG_MAX_Q 4
+#define BD_SEG_MAX_K 5
+#define BD_SEG_FIRST_Q 6
+#define BD_SEG_FIRST_K 7
+#define BD_SEG_MAX_TAIL 8
+#define BD_SEG_KV_NEED_LO 9
+#define BD_SEG_ROW_STATUS 10
+#define BD_SEG_HDR_WORDS 32
+
+/* Word offsets of the regions of the segment table (see bd_attn_seg_layout). */
+#define BD_SEG_OFF_HDR 0        /* [B][32]       per-row header */
+#define BD_SEG_OFF_CU_Q 1       /* [B][L+1]      cu_q: segment starts (local rows), n_real last */
+#define BD_SEG_OFF_CU_K 2       /* [B][L+1]      cu_k: k segment starts - s_first, real_end - s_first last */
+#define BD_SEG_OFF_ROW_LO 3     /* [B][L]        doc start (global) of each local row, -1 on padding */
+#define BD_SEG_OFF_QT_KRANGE 4  /* [B][nqt][2]   per 128-row q tile: first, last 128-row K/V tile (last < first: none) */
+#define BD_SEG_OFF_KT_QRANGE 5  /* [B][nkt][2]   per 128-row K/V tile: first, end (exclusive) local q row attending it */
+#define BD_SEG_OFF_FULL_BITS 6  /* [B][nqt][nkw] bit kt set: tile (qt, kt) is entirely allowed */
+#define BD_SEG_OFF_FWD_WORK 7   /* [B*nqt]       q tiles (b*nqt+qt), most K/V tiles first */
+#define BD_SEG_OFF_BWD_WORK 8   /* [B*nkt]       K/V tiles (b*nkt+kt), most q rows first */
+#define BD_SEG_OFF_COUNTS 9     /* [8]           0: full tiles, 1: partial tiles, 2: empty tiles */
+#define BD_SEG_OFF_TOTAL 10     /* total words */
+#define BD_SEG_NOFF 11
+
+/* Size in bytes of the segment table for this geometry (0 if invalid). */
+size_t bd_attn_seg_bytes(const bd_geom* g);
+
+/* Word offsets of the table regions, BD_SEG_NOFF entries; also writes
+ * offsets[BD_SEG_NOFF..BD_SEG_NOFF+2] = nqt, nkt, nkw. Returns BD_OK or
+ * BD_ERR_ARG. Host only; reads no device memory. */
+int bd_attn_seg_layout(const bd_geom* g, int32_t* offsets /* >= BD_SEG_NOFF + 3 */);
+
+/* Step 1 (per step, shared by every layer): build the varlen segmentation
+ * of the local shard and the 128x128 tile classification.
+ * Reads doc_ids [B, S_full] (device). Writes the segment table `seg`
+ * (device, bd_attn_seg_bytes(g) bytes, caller-owned) and ORs LAYOUT /
+ * KV_RANGE bits into *status (device). Reference: blockdiag_cp.kernels,
+ * `_varlen_seg_for_rank` / `precompute_blockdiag_varlen_meta`; the needed
+ * K/V range from blockdiag_cp.exchange. Segment fields per batch row:
+ * n_real, n_seg, s_first, real_end, cu_q, cu_k, max_q, max_k (bit-exact
+ * with the definition), first_q = cu_q[1], first_k = cu_k[1], max_tail =
+ * largest q segment after the first; an all-padding shard has n_real =
+ * n_seg = 0 and s_first = real_end = row_offset. */
+int bd_attn_seg_build(const int32_t* doc_ids, const bd_geom* g, void* seg, int32_t* status, bd_stream_t stream);
+
+/* Step 2: forward. out = softmax(scale * q k^T + mask) v per query row,
+ * lse = natural-log sum of exp(scale * q.k) over the allowed keys.
+ * Padding rows: out = 0, lse = -inf. Needs the table from
+ * bd_attn_seg_build with the same geometry. Reference:
+ * blockdiag_cp.kernels, `_cp_blockdiag_varlen`; LSE convention from
+ * gemma4_moe.cp_attention, `_scatter_lse`. */
+int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* g, void* out,
+                float* lse, int32_t* status, bd_stream_t stream);
+
+/* Scratch bytes bd_attn_bwd needs in `workspace` (device, caller-owned):
+ * an fp32 dq accumulator [B,Hq,L,D] and delta = rowsum(dout*out) [B,Hq,L]. */
+size_t bd_attn_bwd_workspace_bytes(const bd_geom* g);
+
+/* Step 3: backward of sum(out * dout) from the saved out and lse (no forward
+ * recompute). dq [B,Hq,L,D]; dk, dv [B,Hkv,S_kv,D] summed over the Hq/Hkv
+ * query heads of each group (the all-gather's reduce-scatter(SUM) over
+ * ranks is left to the caller). Padding rows give dq = 0 and contribute
+ * nothing; K/V rows no query attends get 0. grad_dtype: BD_DTYPE_F32 or
+ * BD_DTYPE_BF16 (for all three gradients). Reference: gemma4_moe.
+ * cp_local_ring, `sliding_ring_compute_fa_bwd`; blockdiag_cp.exchange,
+ * `_AllGatherSeqDiff` (sum semantics). */
+int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
+                int32_t* status, bd_stream_t stream);
+
+/* Human-readable text for a host return code. */
+const char* bd_attn_strerror(int code);
+
+/* Test hook for the bounded waits: launches one CTA that waits on an
+ * mbarrier nobody arrives on, with the given limit in nanoseconds, and ORs
+ * BD_STATUS_TIMEOUT into *status when the wait gives up. */
+int bd_attn_selftest_wait_timeout(int32_t* status, uint64_t limit_ns, bd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BDATTN_H */

@@ -1,0 +1,199 @@
+// Host side of the bdattn C ABI: argument checks, TMA tensor maps, launches.
+// The library allocates no device memory and never synchronises a stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace bd {
+cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st);
+cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
+                       const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
+cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const int32_t* seg, const Geom& g, const void* dout, const void* out, const float* lse,
+                       void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st);
+size_t bwd_workspace_bytes(const Geom& g);
+
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nobody arrives on `bar`: the wait must give up after limit_ns
+    if (!mbar_wait(&bar, 0, &abort_flag, nullptr, 0, limit_ns)) atomicOr(status, BD_STATUS_TIMEOUT);
+  }
+}
+}  // namespace bd
+
+using namespace bd;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+  int major = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return BD_ERR_CUDA;
+  return major == 10 ? BD_OK : BD_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int to_geom(const bd_geom* in, Geom* g) {
+  if (!in) return BD_ERR_ARG;
+  if (in->B < 1 || in->Hq < 1 || in->Hkv < 1 || in->Hq % in->Hkv != 0) return BD_ERR_ARG;
+  if (in->D != 64 && in->D != 128 && in->D != 256) return BD_ERR_ARG;
+  if (in->L < 1 || in->S_kv < 1 || in->S_full < 1) return BD_ERR_ARG;
+  if (in->row_offset < 0 || static_cast<long long>(in->row_offset) + in->L > in->S_full) return BD_ERR_ARG;
+  if (in->kv_offset < 0 || static_cast<long long>(in->kv_offset) + in->S_kv > in->S_full) return BD_ERR_ARG;
+  // keep every index the kernels form within 32-bit range
+  if (in->S_full > (1 << 28) || static_cast<long long>(in->B) * in->Hq > (1 << 20)) return BD_ERR_ARG;
+  if (static_cast<long long>(in->B) * (in->L + 1) * 4 + static_cast<long long>(in->B) * in->S_kv > (1LL << 29))
+    return BD_ERR_ARG;
+  if (!(in->scale == in->scale)) return BD_ERR_ARG;  // NaN
+  g->B = in->B;
+  g->Hq = in->Hq;
+  g->Hkv = in->Hkv;
+  g->D = in->D;
+  g->G = in->Hq / in->Hkv;
+  g->S_full = in->S_full;
+  g->L = in->L;
+  g->row_offset = in->row_offset;
+  g->kv_offset = in->kv_offset;
+  g->S_kv = in->S_kv;
+  g->window = in->window > 0 ? in->window : 0;
+  g->scale = in->scale > 0.f ? in->scale : 1.0f / std::sqrt(static_cast<float>(in->D));
+  seg_layout(g->B, g->L, g->S_kv, g->off, &g->nqt, &g->nkt, &g->nkw);
+  return BD_OK;
+}
+
+// 3-D bf16 map over [planes][rows][D] with a (64 x box_rows x 1) box, 128B swizzle;
+// rows past `rows` read as zero.
+int make_map(CUtensorMap* m, const void* ptr, int D, int rows, int planes, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t bd_attn_seg_bytes(const bd_geom* gi) {
+  Geom g;
+  if (to_geom(gi, &g) != BD_OK) return 0;
+  return static_cast<size_t>(g.off[BD_SEG_OFF_TOTAL]) * 4;
+}
+
+int bd_attn_seg_layout(const bd_geom* gi, int32_t* offsets) {
+  Geom g;
+  if (!offsets || to_geom(gi, &g) != BD_OK) return BD_ERR_ARG;
+  for (int i = 0; i < BD_SEG_NOFF; ++i) offsets[i] = g.off[i];
+  offsets[BD_SEG_NOFF] = g.nqt;
+  offsets[BD_SEG_NOFF + 1] = g.nkt;
+  offsets[BD_SEG_NOFF + 2] = g.nkw;
+  return BD_OK;
+}
+
+size_t bd_attn_bwd_workspace_bytes(const bd_geom* gi) {
+  Geom g;
+  if (to_geom(gi, &g) != BD_OK) return 0;
+  return bwd_workspace_bytes(g);
+}
+
+int bd_attn_seg_build(const int32_t* doc_ids, const bd_geom* gi, void* seg, int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!doc_ids || !seg || !status || !aligned16(seg)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_seg_build(doc_ids, g, static_cast<int32_t*>(seg), status, static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,
+                float* lse, int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!q || !k || !v || !seg || !out || !lse || !status) return BD_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(seg)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  if (!load_encode()) return BD_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
+      make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile))
+    return BD_ERR_CUDA;
+  return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status,
+                            static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* seg, const bd_geom* gi, int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
+                int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
+    return BD_ERR_ARG;
+  if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  if (!load_encode()) return BD_ERR_CUDA;
+  CUtensorMap mq, mdo, mk, mv;
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kBwdQ) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kBwdQ) ||
+      make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) || make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile))
+    return BD_ERR_CUDA;
+  return cuda_rc(launch_bwd(mq, mdo, mk, mv, static_cast<const int32_t*>(seg), g, dout, out, lse, dq, dk, dv,
+                            grad_dtype == BD_DTYPE_BF16, workspace, status, static_cast<cudaStream_t>(stream)));
+}
+
+const char* bd_attn_strerror(int code) {
+  switch (code) {
+    case BD_OK: return "ok";
+    case BD_ERR_ARG: return "invalid argument (nothing enqueued)";
+    case BD_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case BD_ERR_UNSUPPORTED: return "device is not a Blackwell sm_10x GPU";
+    default: return "unknown bdattn error code";
+  }
+}
+
+int bd_attn_selftest_wait_timeout(int32_t* status, uint64_t limit_ns, bd_stream_t stream) {
+  if (!status || limit_ns > 2000000000ull) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return cuda_rc(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,581 @@
+// K4a / K4 / K4b: backward of per-document causal attention for one CP shard.
+//
+// Reference (NeMo AutoModel API): gemma4_moe.cp_local_ring
+// `sliding_ring_compute_fa_bwd` -- backward from the saved out / LSE with no
+// forward recompute; blockdiag_cp.exchange `_AllGatherSeqDiff` -- a K/V
+// position's gradient is the sum of every query's contribution. With
+// P = exp(scale q.k - lse) on allowed pairs, delta = rowsum(dout * out):
+//   dV += P^T dO,  dP = dO V^T,  dS = P (dP - delta),
+//   dK += scale dS^T Q,  dQ += scale dS K,
+// dK / dV summed over the Hq/Hkv query heads of a group.
+//
+// K4 design (GB300): one CTA per (128-row K/V tile, kv head), longest first.
+// The CTA keeps K and V in shared memory and loops over the query heads of
+// the group and over the 64-row q tiles that attend its keys. All products
+// are tcgen05 MMAs with fp32 accumulators in tensor memory, computed in the
+// transposed orientation so that the key tile is the M = 128 side:
+//   S^T = K Q^T, dP^T = V dO^T                       (cols [0,64), [64,128))
+//   dV += P^T dO  (P^T bf16 written back over S^T)    (cols [256, 256+Dp))
+//   dK += dS^T Q  (dS^T bf16 in shared memory)        (cols [384, 384+Dp))
+//   dQ^T = K^T dS^T, read out and added to an fp32    (cols [128,192))
+//   accumulator in global memory with red.global.add.
+// dK / dV never leave tensor memory until the last q tile, so the GQA sum is
+// exact and deterministic. For D = 256 the dK / dV columns are produced in
+// two passes of 128 (the S / dP products are recomputed in the second pass)
+// because 2 x 256 fp32 columns would fill the whole tensor memory.
+//   warp 0  loads (TMA for K, V, Q, dO; the q rows' lse / delta / mask bounds)
+//   warp 1  issues the MMAs          warp 2  owns the tensor memory
+//   warps 4-7  P, dS (thread = key row)      warps 8-11  dQ read-out
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "pipeline.cuh"
+
+namespace bd {
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// ----------------------------------------------------------------- K4a
+// delta[row] = sum_d dout[row, d] * out[row, d] (fp32) and dq_acc[row, :] = 0.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ dout,
+                                                      const __nv_bfloat16* __restrict__ out,
+                                                      float* __restrict__ delta, float* __restrict__ dq_acc,
+                                                      long long n_rows, const int32_t* status) {
+  if (*reinterpret_cast<const volatile int*>(status) != 0) return;
+  constexpr int kLanes = D / 8;  // threads per row, 8 elements (16 B) each
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_rows * kLanes;
+       t += nthreads) {
+    const long long row = t / kLanes;
+    const int part = static_cast<int>(t % kLanes);
+    const uint4 a = reinterpret_cast<const uint4*>(dout + row * D)[part];
+    const uint4 o = reinterpret_cast<const uint4*>(out + row * D)[part];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(o2[e]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+#pragma unroll
+    for (int o = kLanes / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, kLanes);
+    if (part == 0) delta[row] = acc;
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ----------------------------------------------------------------- K4b
+// dq = scale * dq_acc in the requested dtype (8 elements per thread).
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
+                                                         long long n_elems, float scale, int to_bf16,
+                                                         const int32_t* status) {
+  if (*reinterpret_cast<const volatile int*>(status) != 0) return;
+  const long long n8 = n_elems / 8;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n8; t += nthreads) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
+    const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
+    if (to_bf16) {
+      uint4 w;
+      w.x = pack_bf16x2(a.x * scale, a.y * scale);
+      w.y = pack_bf16x2(a.z * scale, a.w * scale);
+      w.z = pack_bf16x2(c.x * scale, c.y * scale);
+      w.w = pack_bf16x2(c.z * scale, c.w * scale);
+      reinterpret_cast<uint4*>(dq)[t] = w;
+    } else {
+      reinterpret_cast<float4*>(dq)[2 * t] = make_float4(a.x * scale, a.y * scale, a.z * scale, a.w * scale);
+      reinterpret_cast<float4*>(dq)[2 * t + 1] = make_float4(c.x * scale, c.y * scale, c.z * scale, c.w * scale);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ K4
+template <int D, int NSQ>
+struct BwdSmem {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kKChunk = kTile * 128;  // 128 rows x 128 B
+  static constexpr int kQChunk = kBwdQ * 128;  // 64 rows x 128 B
+  // v must directly follow k: for D = 64 the dQ^T product reads A rows
+  // 64..127 (d >= 64, discarded) from the 16 KB after k.
+  alignas(1024) uint8_t k[kChunks][kKChunk];
+  alignas(1024) uint8_t v[kChunks][kKChunk];
+  alignas(1024) uint8_t q[NSQ][kChunks][kQChunk];
+  alignas(1024) uint8_t dout[NSQ][kChunks][kQChunk];
+  alignas(1024) uint8_t ds[kKChunk];  // dS^T, 128 keys x 64 q, bf16, 128B-swizzled
+  float lse2[NSQ][kBwdQ];
+  float delta[NSQ][kBwdQ];
+  int jlo[NSQ][kBwdQ];
+  int jhi[NSQ][kBwdQ];
+  uint64_t kv_full, q_full[NSQ], q_empty[NSQ];
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int b, kt, q64_lo, nq64, n_real, skip;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kDp = D < 128 ? D : 128;  // dK / dV columns per pass
+  static constexpr int kPasses = D / kDp;
+  static constexpr int kNsq = D == 256 ? 1 : (D == 128 ? 2 : 3);
+  static constexpr uint32_t kColS = 0, kColDp = 64, kColDq = 128, kColDv = 256, kColDk = 384;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
+               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
+               const float* __restrict__ delta, float* __restrict__ dq_acc, void* __restrict__ dk,
+               void* __restrict__ dv, int grads_bf16, int32_t* status) {
+  using Cfg = BwdCfg<D>;
+  constexpr int NSQ = Cfg::kNsq, kDp = Cfg::kDp, kPasses = Cfg::kPasses;
+  using Smem = BwdSmem<D, NSQ>;
+  constexpr int kChunks = Smem::kChunks;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hk = blockIdx.x % g.Hkv;
+  volatile int* vstatus = status;
+
+  if (tid == 0) {
+    const int item = blockIdx.x / g.Hkv;
+    const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
+    int ok = wi >= 0 && wi < g.B * g.nkt;
+    const int b = ok ? wi / g.nkt : 0, kt = ok ? wi % g.nkt : 0;
+    const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+    ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
+         hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
+         hdr[kHdrSfull] == g.S_full;
+    const int n_real = hdr[BD_SEG_N_REAL];
+    const int32_t* qr = seg + g.off[BD_SEG_OFF_KT_QRANGE] + (b * g.nkt + kt) * 2;
+    const int qlo = qr[0], qhi = qr[1];
+    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real;
+    const int nq64 = qhi > qlo ? (qhi - 1) / kBwdQ - qlo / kBwdQ + 1 : 0;
+    if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
+    s.b = b;
+    s.kt = kt;
+    s.q64_lo = qlo / kBwdQ;
+    s.nq64 = nq64;
+    s.n_real = n_real;
+    s.skip = (!ok || *vstatus != 0) ? 1 : 0;
+    s.abort_flag = 0;
+    mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < NSQ; ++i) {
+      mbar_init(&s.q_full[i], 1);
+      mbar_init(&s.q_empty[i], 1);
+    }
+    mbar_init(&s.s_full, 1);
+    mbar_init(&s.dp_full, 1);
+    mbar_init(&s.p_full, 128);
+    mbar_init(&s.ds_full, 128);
+    mbar_init(&s.ds_empty, 1);
+    mbar_init(&s.dq_full, 1);
+    mbar_init(&s.dq_empty, 128);
+    mbar_init(&s.acc_full, 1);
+    mbar_init(&s.acc_empty, 128);
+    mbar_init(&s.mma_drain, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (s.skip) return;
+  const int b = s.b, kt = s.kt, q64_lo = s.q64_lo, nq64 = s.nq64, n_real = s.n_real;
+  const int G = g.G;
+  const int n_it_pass = G * nq64;
+  const int n_it = kPasses * n_it_pass;
+  const size_t kv_row0 = (static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv;
+
+  auto store_row = [&](void* base, size_t elem_off, const float* vals32) {
+    if (grads_bf16) {
+      uint4* p = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(base) + elem_off);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint4 w;
+        w.x = pack_bf16x2(vals32[8 * e + 0], vals32[8 * e + 1]);
+        w.y = pack_bf16x2(vals32[8 * e + 2], vals32[8 * e + 3]);
+        w.z = pack_bf16x2(vals32[8 * e + 4], vals32[8 * e + 5]);
+        w.w = pack_bf16x2(vals32[8 * e + 6], vals32[8 * e + 7]);
+        p[e] = w;
+      }
+    } else {
+      float4* p = reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + elem_off);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        p[e] = make_float4(vals32[4 * e + 0], vals32[4 * e + 1], vals32[4 * e + 2], vals32[4 * e + 3]);
+    }
+  };
+
+  if (n_it == 0) {
+    // No query attends this K/V tile: its dK / dV rows are zero.
+    if (warp >= 4 && warp < 8) {
+      const int j = kt * kTile + (tid - 128);
+      if (j < g.S_kv) {
+        float z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0.f;
+        for (int c = 0; c < D; c += 32) {
+          store_row(dk, (kv_row0 + j) * D + c, z);
+          store_row(dv, (kv_row0 + j) * D + c, z);
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == 2) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+
+  auto decode = [&](int it, int& pass, int& h, int& q0) {
+    pass = it / n_it_pass;
+    const int rem = it - pass * n_it_pass;
+    const int gq = rem / nq64;
+    h = hk * G + gq;
+    q0 = (q64_lo + rem - gq * nq64) * kBwdQ;
+  };
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- loads
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_dout);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&s.kv_full, 2 * kChunks * Smem::kKChunk);
+      for (int c = 0; c < kChunks; ++c) {
+        tma_load_3d(s.k[c], &tm_k, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
+        tma_load_3d(s.v[c], &tm_v, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
+      }
+    }
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ, n = it / NSQ;
+      if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
+      int pass, h, q0;
+      decode(it, pass, h, q0);
+      for (int c = lane; c < kBwdQ; c += 32) {
+        const int i = q0 + c;
+        float l2 = 0.f, dl = 0.f;
+        int lo = 1, hi = 0;
+        if (i < n_real) {
+          const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
+          l2 = lse[row] * 1.4426950408889634f;
+          dl = delta[row];
+          const int p = g.row_offset + i;
+          lo = row_lo_window(seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i], p, g.window) - g.kv_offset;
+          hi = p - g.kv_offset;
+        }
+        s.lse2[st][c] = l2;
+        s.delta[st][c] = dl;
+        s.jlo[st][c] = lo;
+        s.jhi[st][c] = hi;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&s.q_full[st], 2 * kChunks * Smem::kQChunk);
+        for (int c = 0; c < kChunks; ++c) {
+          tma_load_3d(s.q[st][c], &tm_q, &s.q_full[st], c * 64, q0, b * g.Hq + h);
+          tma_load_3d(s.dout[st][c], &tm_dout, &s.q_full[st], c * 64, q0, b * g.Hq + h);
+        }
+      }
+      ++issued;
+    }
+    if (lane == 0) {
+      if (issued < n_it) {
+        s.abort_flag = 1;
+        atomicOr(status, BD_STATUS_TIMEOUT);
+      }
+      mbar_wait_drain(&s.kv_full, 0);
+      for (int it = (issued > NSQ ? issued - NSQ : 0); it < issued; ++it)
+        mbar_wait_drain(&s.q_full[it % NSQ], (it / NSQ) & 1);
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idST = idesc_bf16(128, kBwdQ, false, false);
+      constexpr uint32_t idDKV = idesc_bf16(128, kDp, false, true);
+      constexpr uint32_t idDQ = idesc_bf16(128, kBwdQ, true, true);
+      auto issue_st = [&](uint32_t col, uint8_t (*a)[Smem::kKChunk], uint8_t (*bq)[Smem::kQChunk]) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int ch = ks >> 2, kk = ks & 3;
+          const uint64_t da = umma_desc_sw128(smem_u32(a[ch]) + kk * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(smem_u32(bq[ch]) + kk * 32, 16, 1024);
+          umma_ss(tbase + col, da, db, idST, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        return pipe_wait(bar, par, &s.abort_flag, vstatus);
+      };
+      bool ok = wait(&s.kv_full, 0) && wait(&s.q_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_st(Cfg::kColS, s.k, s.q[0]);
+        umma_commit(&s.s_full);
+        issue_st(Cfg::kColDp, s.v, s.dout[0]);
+        umma_commit(&s.dp_full);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % NSQ;
+        int pass, h, q0;
+        decode(it, pass, h, q0);
+        const bool first_of_pass = (it % n_it_pass) == 0;
+        const bool last_of_pass = (it % n_it_pass) == n_it_pass - 1;
+        if (first_of_pass && pass > 0 && !wait(&s.acc_empty, (pass - 1) & 1)) { ok = false; break; }
+        // dV += P^T dO[:, pass]
+        if (!wait(&s.p_full, it & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kBwdQ / 16; ++ks) {
+          const uint64_t db = umma_desc_sw128(smem_u32(s.dout[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
+          umma_ts(tbase + Cfg::kColDv, tbase + Cfg::kColS + ks * 8, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
+        }
+        if (NSQ > 1 && it + 1 < n_it) {
+          const int st1 = (it + 1) % NSQ;
+          if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_st(Cfg::kColS, s.k, s.q[st1]);
+          umma_commit(&s.s_full);
+        }
+        // dK += dS^T Q[:, pass] ; dQ^T = K[:, pass]^T dS^T
+        if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kBwdQ / 16; ++ks) {
+          const uint64_t da = umma_desc_sw128(smem_u32(s.ds) + ks * 32, 16, 1024);
+          const uint64_t db = umma_desc_sw128(smem_u32(s.q[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
+          umma_ss(tbase + Cfg::kColDk, da, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
+        }
+        if (it > 0 && !wait(&s.dq_empty, (it - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTile / 16; ++ks) {
+          const uint64_t da = umma_desc_sw128(smem_u32(s.k[pass * (kDp / 64)]) + ks * 2048, Smem::kKChunk, 1024);
+          const uint64_t db = umma_desc_sw128(smem_u32(s.ds) + ks * 2048, Smem::kKChunk, 1024);
+          umma_ss(tbase + Cfg::kColDq, da, db, idDQ, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(&s.dq_full);
+        umma_commit(&s.ds_empty);
+        umma_commit(&s.q_empty[st]);
+        if (last_of_pass) umma_commit(&s.acc_full);
+        if (it + 1 < n_it) {
+          const int st1 = (it + 1) % NSQ;
+          if (NSQ == 1) {
+            if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_st(Cfg::kColS, s.k, s.q[st1]);
+            umma_commit(&s.s_full);
+          }
+          issue_st(Cfg::kColDp, s.v, s.dout[st1]);
+          umma_commit(&s.dp_full);
+        }
+      }
+      if (!ok) {
+        s.abort_flag = 1;
+        atomicOr(status, BD_STATUS_TIMEOUT);
+      }
+      umma_commit(&s.mma_drain);
+      mbar_wait_drain(&s.mma_drain, 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------ P and dS (key rows)
+    const int r = tid - 128;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int j = kt * kTile + r;  // K/V buffer row of this thread
+    const float sl2 = g.scale * 1.4426950408889634f;
+    uint8_t* ds_row = s.ds + r * 128;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSQ;
+      int pass, h, q0;
+      decode(it, pass, h, q0);
+      if (!warp_wait(&s.q_full[st], (it / NSQ) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      if (!warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[64];
+      tmem_ld32(tbase + lane_off + Cfg::kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tbase + lane_off + Cfg::kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld();
+      const bool all_real = q0 + kBwdQ - 1 < n_real;
+      const bool full = all_real && s.jlo[st][kBwdQ - 1] <= j && j <= s.jhi[st][0];
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool allowed = full || (s.jlo[st][c] <= j && j <= s.jhi[st][c]);
+        p[c] = allowed ? fast_exp2(__uint_as_float(sr[c]) * sl2 - s.lse2[st][c]) : 0.f;
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      tmem_st32(tbase + lane_off + Cfg::kColS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+
+      if (!warp_wait(&s.dp_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld32(tbase + lane_off + Cfg::kColDp, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tbase + lane_off + Cfg::kColDp + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float d0 = p[2 * c] * (__uint_as_float(sr[2 * c]) - s.delta[st][2 * c]);
+        const float d1 = p[2 * c + 1] * (__uint_as_float(sr[2 * c + 1]) - s.delta[st][2 * c + 1]);
+        pk[c] = pack_bf16x2(d0, d1);
+      }
+      if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      // 128 B row of dS^T in the 128B-swizzled K-major layout
+#pragma unroll
+      for (int c16 = 0; c16 < 8; ++c16) {
+        uint4 w = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        *reinterpret_cast<uint4*>(ds_row + ((c16 ^ (r & 7)) << 4)) = w;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&s.ds_full);
+
+      if ((it % n_it_pass) == n_it_pass - 1) {
+        // end of a pass: write this thread's dK / dV row (columns of the pass)
+        if (!warp_wait(&s.acc_full, pass & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kDp; c += 32) {
+          uint32_t vv[32];
+          float f[32];
+          tmem_ld32(tbase + lane_off + Cfg::kColDv + c, vv);
+          tmem_wait_ld();
+          if (j < g.S_kv) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);
+            store_row(dv, (kv_row0 + j) * D + pass * kDp + c, f);
+          }
+          tmem_ld32(tbase + lane_off + Cfg::kColDk + c, vv);
+          tmem_wait_ld();
+          if (j < g.S_kv) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * g.scale;
+            store_row(dk, (kv_row0 + j) * D + pass * kDp + c, f);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&s.acc_empty);
+      }
+    }
+    if (!ok) {
+      s.abort_flag = 1;
+      if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
+    }
+  } else if (warp >= 8) {
+    // ----------------------------------------------- dQ read-out (d rows)
+    const int r = tid - 256;  // d index within the pass == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool active = (warp & 3) * 32 < kDp;  // D = 64: lanes 64..127 hold nothing useful
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      int pass, h, q0;
+      decode(it, pass, h, q0);
+      if (!warp_wait(&s.dq_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t qv[64];
+      if (active) {
+        tmem_ld32(tbase + lane_off + Cfg::kColDq, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+        tmem_ld32(tbase + lane_off + Cfg::kColDq + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(&s.dq_empty);
+      if (active) {
+        float* base = dq_acc + ((static_cast<size_t>(b) * g.Hq + h) * g.L) * D + pass * kDp + r;
+        const int cmax = min(kBwdQ, n_real - q0);
+#pragma unroll
+        for (int c = 0; c < kBwdQ; ++c)
+          if (c < cmax) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+      }
+    }
+    if (!ok) {
+      s.abort_flag = 1;
+      if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const int32_t* seg, const Geom& g, const __nv_bfloat16* dout, const __nv_bfloat16* out,
+                         const float* lse, void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status,
+                         cudaStream_t st) {
+  const long long rows = static_cast<long long>(g.B) * g.Hq * g.L;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(static_cast<size_t>(rows) * D * 4));
+  {
+    const long long blocks = (rows * (D / 8) + 255) / 256;
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
+    bwd_pre_kernel<D><<<grid, 256, 0, st>>>(dout, out, delta, dq_acc, rows, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const size_t smem = sizeof(BwdSmem<D, BwdCfg<D>::kNsq>) + 1024;  // + 1 KB to align the swizzled tiles
+    auto kern = bwd_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
+    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kern<<<static_cast<unsigned>(grid), 384, smem, st>>>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16,
+                                                         status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long n = rows * D;
+    const long long blocks = (n / 8 + 255) / 256;
+    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
+    dq_convert_kernel<<<grid, 256, 0, st>>>(dq_acc, dq, n, g.scale, bf16, status);
+  }
+  return cudaGetLastError();
+}
+}  // namespace
+
+size_t bwd_workspace_bytes(const Geom& g) {
+  const size_t rows = static_cast<size_t>(g.B) * g.Hq * g.L;
+  return align256(rows * g.D * 4) + align256(rows * 4);
+}
+
+// K4a (delta, zero the dq accumulator) -> K4 (dK, dV, dq accumulation) -> K4b (dq).
+cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
+                       const int32_t* seg, const Geom& g, const void* dout, const void* out, const float* lse,
+                       void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
+  const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
+  const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(out);
+  switch (g.D) {
+    case 64: return launch_bwd_d<64>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
+    case 128: return launch_bwd_d<128>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
+    case 256: return launch_bwd_d<256>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace bd

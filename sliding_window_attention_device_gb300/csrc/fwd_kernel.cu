@@ -1,0 +1,404 @@
+// K3: forward of per-document causal attention for one CP query shard.
+//
+// What it computes (NeMo AutoModel API, blockdiag_cp.kernels
+// `_cp_blockdiag_varlen`): for every real local row p, the softmax over the
+// allowed keys [lo(p), p] (lo = max(doc_start, p - W + 1)) of scale * q.k,
+// times V; LSE = natural-log sum-exp (gemma4_moe.cp_attention `_scatter_lse`:
+// -inf on rows that take no part). Padding rows return zeros.
+//
+// Design (GB300): one CTA per (128-row q tile, pair of query heads of the same
+// GQA group); the work list puts the q tiles with the most K/V tiles first.
+//   warp 0      TMA producer: Q tiles once, then K and V tiles of the tile's
+//               contiguous K/V range through an NS-stage ring (128B swizzle).
+//   warp 1      one thread issues tcgen05.mma: S = Q K^T into TMEM, and
+//               O += P V with P read from TMEM (the "TS" form).
+//   warp 2      allocates / frees tensor memory.
+//   warps 4..   one warpgroup per q tile: each thread owns one row; reads S
+//               from TMEM, applies the mask only on partial tiles, keeps the
+//               running max / sum in fp32, writes P (bf16) over S in TMEM,
+//               rescales O only when the max grows by more than 2^8, and
+//               finally normalises O and writes out / LSE.
+// The two q tiles of a CTA share every K/V tile (same kv head), so the tensor
+// core works on one while the other's softmax runs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "pipeline.cuh"
+
+namespace bd {
+
+template <int D, int NQ, int NS>
+struct FwdSmem {
+  static constexpr int kChunks = D / 64;         // 64-column (128 B) chunks per row
+  static constexpr int kChunkBytes = kTile * 128;  // 128 rows x 128 B
+  alignas(1024) uint8_t q[NQ][kChunks][kChunkBytes];
+  alignas(1024) uint8_t k[NS][kChunks][kChunkBytes];
+  alignas(1024) uint8_t v[NS][kChunks][kChunkBytes];
+  uint64_t q_full;
+  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
+  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
+  uint64_t mma_drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  // work item, decoded by thread 0
+  int b, qt, kt_lo, nk, n_real, skip;
+};
+
+template <int D, int NQ>
+struct FwdTmem {
+  __host__ __device__ static constexpr int kS(int qi) { return qi * 128; }
+  __host__ __device__ static constexpr int kO(int qi) { return NQ * 128 + qi * D; }
+  static constexpr int kUsed = NQ * (128 + D);
+  static constexpr int kCols = kUsed <= 32 ? 32 : kUsed <= 64 ? 64 : kUsed <= 128 ? 128 : kUsed <= 256 ? 256 : 512;
+  static_assert(kUsed <= 512, "tensor memory budget");
+};
+
+template <int D, int NQ, int NS>
+__global__ void __launch_bounds__(128 + NQ * 128, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
+               __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t* status) {
+  using Smem = FwdSmem<D, NQ, NS>;
+  using TM = FwdTmem<D, NQ>;
+  constexpr int kChunks = Smem::kChunks;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_pairs = g.Hq / NQ;
+  const int pair = blockIdx.x % n_pairs;
+  volatile int* vstatus = status;
+
+  if (tid == 0) {
+    const int item = blockIdx.x / n_pairs;
+    const int wi = seg[g.off[BD_SEG_OFF_FWD_WORK] + item];
+    int ok = wi >= 0 && wi < g.B * g.nqt;
+    const int b = ok ? wi / g.nqt : 0, qt = ok ? wi % g.nqt : 0;
+    const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+    ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
+         hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
+         hdr[kHdrSfull] == g.S_full;
+    const int n_real = hdr[BD_SEG_N_REAL];
+    const int32_t* kr = seg + g.off[BD_SEG_OFF_QT_KRANGE] + (b * g.nqt + qt) * 2;
+    const int kt_lo = kr[0], kt_hi = kr[1];
+    const int nk = kt_hi >= kt_lo ? kt_hi - kt_lo + 1 : 0;
+    ok = ok && n_real >= 0 && n_real <= g.L && (nk == 0 || (kt_lo >= 0 && kt_hi < g.nkt));
+    if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
+    s.b = b;
+    s.qt = qt;
+    s.kt_lo = kt_lo;
+    s.nk = nk;
+    s.n_real = n_real;
+    s.skip = (!ok || *vstatus != 0) ? 1 : 0;
+    s.abort_flag = 0;
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&s.k_full[i], 1);
+      mbar_init(&s.k_empty[i], 1);
+      mbar_init(&s.v_full[i], 1);
+      mbar_init(&s.v_empty[i], 1);
+    }
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.o_done[i], 1);
+    }
+    mbar_init(&s.q_full, 1);
+    mbar_init(&s.mma_drain, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (s.skip) return;
+  const int b = s.b, qt = s.qt, kt_lo = s.kt_lo, nk = s.nk, n_real = s.n_real;
+  const int h0 = pair * NQ, hk = h0 / g.G;
+
+  if (nk == 0) {
+    // No real row in this q tile: zeros and -inf.
+    if (tid >= 128) {
+      const int qi = (tid - 128) >> 7, r = (tid - 128) & 127;
+      const int i = qt * kTile + r;
+      if (i < g.L) {
+        const size_t row = (static_cast<size_t>(b) * g.Hq + h0 + qi) * g.L + i;
+        uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
+        for (int c = 0; c < D / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+        lse[row] = -INFINITY;
+      }
+    }
+    return;
+  }
+
+  if (warp == 2) {
+    tmem_alloc(&s.tmem_base, TM::kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    mbar_arrive_expect_tx(&s.q_full, NQ * kChunks * Smem::kChunkBytes);
+    for (int qi = 0; qi < NQ; ++qi)
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.q[qi][c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h0 + qi);
+    int k_issued = 0, v_issued = 0;
+    for (int j = 0; j < nk; ++j) {
+      const int st = j % NS, n = j / NS;
+      if (j >= NS && !pipe_wait(&s.k_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
+        break;
+      mbar_arrive_expect_tx(&s.k_full[st], kChunks * Smem::kChunkBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.k[st][c], &tm_k, &s.k_full[st], c * 64, (kt_lo + j) * kTile, b * g.Hkv + hk);
+      ++k_issued;
+      if (j >= NS && !pipe_wait(&s.v_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
+        break;
+      mbar_arrive_expect_tx(&s.v_full[st], kChunks * Smem::kChunkBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.v[st][c], &tm_v, &s.v_full[st], c * 64, (kt_lo + j) * kTile, b * g.Hkv + hk);
+      ++v_issued;
+    }
+    if (v_issued < nk) {
+      s.abort_flag = 1;
+      atomicOr(status, BD_STATUS_TIMEOUT);
+    }
+    // make sure no copy into this CTA's shared memory is still in flight at exit
+    mbar_wait_drain(&s.q_full, 0);
+    for (int j = (k_issued > NS ? k_issued - NS : 0); j < k_issued; ++j) mbar_wait_drain(&s.k_full[j % NS], (j / NS) & 1);
+    for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j) mbar_wait_drain(&s.v_full[j % NS], (j / NS) & 1);
+  } else if (warp == 1 && lane == 0) {
+    // ----------------------------------------------------------- MMA issuer
+    constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+    auto issue_s = [&](int qi, int st) {
+      const uint32_t d = tbase + TM::kS(qi);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int ch = ks >> 2, kk = ks & 3;
+        const uint64_t a = umma_desc_sw128(smem_u32(s.q[qi][ch]) + kk * 32, 16, 1024);
+        const uint64_t bb = umma_desc_sw128(smem_u32(s.k[st][ch]) + kk * 32, 16, 1024);
+        umma_ss(d, a, bb, idS, ks > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int qi, int st, bool acc) {
+      const uint32_t d = tbase + TM::kO(qi);
+#pragma unroll
+      for (int ks = 0; ks < kTile / 16; ++ks) {
+        const uint64_t bb = umma_desc_sw128(smem_u32(s.v[st][0]) + ks * 2048, Smem::kChunkBytes, 1024);
+        umma_ts(d, tbase + TM::kS(qi) + ks * 8, bb, idPV, (acc || ks > 0) ? 1u : 0u);
+      }
+    };
+    bool ok = pipe_wait(&s.q_full, 0, &s.abort_flag, vstatus) &&
+              pipe_wait(&s.k_full[0], 0, &s.abort_flag, vstatus);
+    if (ok) {
+      tc_fence_after();
+      for (int qi = 0; qi < NQ; ++qi) {
+        issue_s(qi, 0);
+        umma_commit(&s.s_full[qi]);
+      }
+      umma_commit(&s.k_empty[0]);
+    }
+    for (int j = 0; ok && j < nk; ++j) {
+      const int st = j % NS;
+      if (!pipe_wait(&s.v_full[st], (j / NS) & 1, &s.abort_flag, vstatus)) {
+        ok = false;
+        break;
+      }
+      for (int qi = 0; qi < NQ; ++qi) {
+        if (!pipe_wait(&s.p_full[qi], j & 1, &s.abort_flag, vstatus)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(qi, st, j > 0);
+        umma_commit(&s.o_done[qi]);
+        if (j + 1 < nk) {
+          const int st1 = (j + 1) % NS;
+          if (qi == 0 &&
+              !pipe_wait(&s.k_full[st1], ((j + 1) / NS) & 1, &s.abort_flag, vstatus)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(qi, st1);
+          umma_commit(&s.s_full[qi]);
+        }
+      }
+      if (!ok) break;
+      umma_commit(&s.v_empty[st]);
+      if (j + 1 < nk) umma_commit(&s.k_empty[(j + 1) % NS]);
+    }
+    if (!ok) {
+      s.abort_flag = 1;
+      atomicOr(status, BD_STATUS_TIMEOUT);
+    }
+    umma_commit(&s.mma_drain);
+    mbar_wait_drain(&s.mma_drain, 0);
+  } else if (warp >= 4) {
+    // ------------------------------------------------- softmax warpgroups
+    const int qi = (warp - 4) >> 2;
+    const int r = tid - 128 - qi * 128;          // row within the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tbase + lane_off + TM::kS(qi);
+    const uint32_t t_o = tbase + lane_off + TM::kO(qi);
+    const int h = h0 + qi;
+    const int i = qt * kTile + r;
+    const bool real = i < n_real;
+    int jlo = 1, jhi = 0;  // allowed K/V buffer rows [jlo, jhi] of this row
+    if (real) {
+      const int p = g.row_offset + i;
+      const int doc_start = seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i];
+      jlo = row_lo_window(doc_start, p, g.window) - g.kv_offset;
+      jhi = p - g.kv_offset;
+    }
+    const float sl2 = g.scale * 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nk; ++j) {
+      if (!warp_wait(&s.s_full[qi], j & 1, &s.abort_flag, vstatus)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t xr[128];
+      tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
+      tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
+      tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&xr[64]));
+      tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
+      tmem_wait_ld();
+      const int c0 = (kt_lo + j) * kTile;
+      float x[128];
+      float tmax = -INFINITY;
+      if (jlo <= c0 && c0 + kTile - 1 <= jhi) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          x[c] = __uint_as_float(xr[c]) * sl2;
+          tmax = fmaxf(tmax, x[c]);
+        }
+      } else {
+        const int a = jlo - c0, e = jhi - c0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          x[c] = (c >= a && c <= e) ? __uint_as_float(xr[c]) * sl2 : -INFINITY;
+          tmax = fmaxf(tmax, x[c]);
+        }
+      }
+      const float m_new = fmaxf(m, tmax);
+      const bool need = m_new > m + 8.0f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_exp2(m - m_new) : 1.0f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
+        }
+        if (j > 0) {
+          if (!warp_wait(&s.o_done[qi], (j - 1) & 1, &s.abort_flag, vstatus)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      const float mm = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = fast_exp2(x[2 * c] - mm), p1 = fast_exp2(x[2 * c + 1] - mm);
+        rs += p0 + p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l += rs;
+      tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[qi]);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !warp_wait(&s.o_done[qi], (nk - 1) & 1, &s.abort_flag, vstatus)) ok = false;
+    if (!ok) {
+      s.abort_flag = 1;
+      if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
+    } else {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const float lse_v = (real && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
+      uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c, o);
+        tmem_wait_ld();
+        if (i < g.L) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+            o4[c / 8 + e] = w;
+          }
+        }
+      }
+      if (i < g.L) lse[row] = lse_v;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TM::kCols);
+  }
+}
+
+template <int D, int NQ, int NS>
+static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                              const int32_t* seg, const Geom& g, __nv_bfloat16* out, float* lse, int32_t* status,
+                              cudaStream_t st) {
+  const size_t smem = sizeof(FwdSmem<D, NQ, NS>) + 1024;  // + 1 KB to align the swizzled tiles
+  auto kern = fwd_kernel<D, NQ, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), 128 + NQ * 128, smem, st>>>(mq, mk, mv, seg, g, out, lse, status);
+  return cudaGetLastError();
+}
+
+// Two query heads of one GQA group per CTA when the group size is even and
+// D <= 128 (tensor memory: 2 x (128 + D) columns); one otherwise.
+cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
+                       const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st) {
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  const bool pairs = (g.G % 2) == 0;
+  switch (g.D) {
+    case 64:
+      return pairs ? launch_one<64, 2, 3>(mq, mk, mv, seg, g, o, lse, status, st)
+                   : launch_one<64, 1, 3>(mq, mk, mv, seg, g, o, lse, status, st);
+    case 128:
+      return pairs ? launch_one<128, 2, 2>(mq, mk, mv, seg, g, o, lse, status, st)
+                   : launch_one<128, 1, 2>(mq, mk, mv, seg, g, o, lse, status, st);
+    case 256:
+      return launch_one<256, 1, 1>(mq, mk, mv, seg, g, o, lse, status, st);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace bd
