@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of per-document causal (block-diagonal) CP attention, forward + backward.
+
+Metric: fwd+bwd TFLOP/s counting only unmasked FLOPs (4*D per allowed
+(query, key) pair per query head forward, 10*D backward), and the fraction of
+the GB300's measured dense BF16 peak, on one GPU.
+
+Workload (default): the packed multi-document 32K shard set -- B=2, Hq=32,
+Hkv=8, D=128, S=32768 split into 8 virtual context-parallel ranks (L=4096),
+K/V = the full sequence. One step runs the whole path for every rank:
+segmentation + tile classification, forward, backward (prep, main, dq
+finalize). Inputs are resident in HBM before the timed region; K/V (268 MB)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+With --gpus N (torchrun), each GPU runs an independent replica with its own
+seed (weak scaling; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sliding_window_attention_device_gb300 import synth  # noqa: E402
+
+METRIC = "fwd+bwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak, 1 GPU"
+UNIT = "TFLOP/s"
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward main
+# kernel, from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (see
+# profiles/), valid only for the kernel source with this sha256 prefix.
+TRAFFIC = {"kernel": "bwd_kernel<128>", "source_sha256": None, "bytes_per_launch": None}
+
+
+# ------------------------------------------------------------------ workload
+def doc_starts(row: np.ndarray) -> np.ndarray:
+    """Global start position of the run each position belongs to."""
+    n = row.shape[0]
+    change = np.ones(n, bool)
+    change[1:] = row[1:] != row[:-1]
+    return np.maximum.accumulate(np.where(change, np.arange(n), 0))
+
+
+def pairs_closed_form(doc: np.ndarray, row_offset: int, L: int, window: int) -> int:
+    """Allowed (query, key) pairs over real local rows: each real row p attends
+    [max(doc_start(p), p - W + 1), p], so it contributes p - lo + 1 keys."""
+    total = 0
+    for b in range(doc.shape[0]):
+        st = doc_starts(doc[b])
+        p = row_offset + np.arange(L)
+        lo = st[p]
+        if window > 0:
+            lo = np.maximum(lo, p - window + 1)
+        real = doc[b, p] != 0
+        total += int(((p - lo + 1) * real).sum())
+    return total
+
+
+def needed_range(doc: np.ndarray, row_offset: int, L: int) -> tuple[int, int]:
+    """[min_b s_first, max_b real_end) of a shard (the needed-only K/V range)."""
+    lo, hi = None, None
+    for b in range(doc.shape[0]):
+        p = row_offset + np.arange(L)
+        real = doc[b, p] != 0
+        n_real = int(np.argmin(real)) if not real.all() else L
+        if n_real == 0:
+            continue
+        s_first = int(doc_starts(doc[b])[row_offset])
+        lo = s_first if lo is None else min(lo, s_first)
+        hi = row_offset + n_real if hi is None else max(hi, row_offset + n_real)
+    if lo is None:
+        return row_offset, 1
+    return lo, hi - lo
+
+
+def shard_plan(w: synth.Workload, doc: np.ndarray):
+    plan = []
+    for r in w.ranks:
+        ro = r * w.L
+        if w.kv == "needed":
+            kvo, skv = needed_range(doc, ro, w.L)
+        else:
+            kvo, skv = w.prefix_kv(r)
+        plan.append(dict(r=r, row_offset=ro, kv_offset=kvo, S_kv=skv,
+                         pairs=pairs_closed_form(doc, ro, w.L, w.window)))
+    return plan
+
+
+# ------------------------------------------------------------------- helpers
+def read_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(source="measured", bf16_tflops=d.get("bf16_tflops"),
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), hbm_gbs=d.get("hbm_gbs"))
+    return dict(source="fallback", bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, hbm_gbs=6800.0)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.index)], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_sha() -> str:
+    p = os.path.join(ROOT, "sliding_window_attention_device_gb300", "csrc", "bwd_kernels.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+# --------------------------------------------------------------- our path
+class Replica:
+    """Device-resident inputs / outputs of every shard of the workload."""
+
+    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None):
+        from sliding_window_attention_device_gb300 import bdattn
+        self.bd, self.w, self.dev, self.grad_dtype = bdattn, w, dev, grad_dtype
+        self.doc_np = synth.doc_layout(w.layout, w.B, w.S, seed)
+        self.plan = [sh for sh in shard_plan(w, self.doc_np) if ranks is None or sh["r"] in ranks]
+        self.doc = torch.from_numpy(self.doc_np).to(dev)
+        k, v = synth.kv_rows(w, seed)
+        self.k_full, self.v_full = k.to(dev), v.to(dev)
+        self.status = bdattn.new_status(dev)
+        self.shards = []
+        ws = 0
+        for sh in self.plan:
+            g = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, sh["row_offset"], sh["kv_offset"], sh["S_kv"], w.window)
+            a, b = sh["kv_offset"], sh["kv_offset"] + sh["S_kv"]
+            k_sh = self.k_full if (a, b) == (0, w.S) else self.k_full[:, :, a:b].contiguous()
+            v_sh = self.v_full if (a, b) == (0, w.S) else self.v_full[:, :, a:b].contiguous()
+            d = dict(g=g, pairs=sh["pairs"], k=k_sh, v=v_sh,
+                     q=synth.q_shard(w, sh["r"], seed).to(dev), do=synth.dout_shard(w, sh["r"], seed).to(dev),
+                     seg=torch.empty(bdattn.seg_bytes(g) // 4, dtype=torch.int32, device=dev),
+                     out=torch.empty(w.B, w.Hq, w.L, w.D, dtype=torch.bfloat16, device=dev),
+                     lse=torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev),
+                     dq=torch.empty(w.B, w.Hq, w.L, w.D, dtype=grad_dtype, device=dev),
+                     dk=torch.empty(w.B, w.Hkv, sh["S_kv"], w.D, dtype=grad_dtype, device=dev),
+                     dv=torch.empty(w.B, w.Hkv, sh["S_kv"], w.D, dtype=grad_dtype, device=dev))
+            ws = max(ws, bdattn.bwd_workspace_bytes(g))
+            self.shards.append(d)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 6 * len(self.shards)
+
+    def flops(self) -> tuple[float, float, float]:
+        D, Hq = self.w.D, self.w.Hq
+        pairs = sum(s["pairs"] for s in self.shards)
+        return 14.0 * D * Hq * pairs, 4.0 * D * Hq * pairs, 10.0 * D * Hq * pairs
+
+    def step(self, ev=None):
+        bd = self.bd
+        for i, s in enumerate(self.shards):
+            g = s["g"]
+            ws = self.workspace[:bd.bwd_workspace_bytes(g)]
+            bd.bd_attn_seg_build(self.doc, g, seg=s["seg"], status=self.status)
+            if ev is not None:
+                ev["fwd"][i][0].record()
+            bd.bd_attn_fwd(s["q"], s["k"], s["v"], s["seg"], g, self.status, out=s["out"], lse=s["lse"])
+            if ev is not None:
+                ev["fwd"][i][1].record()
+            bd.bd_attn_bwd_prep(s["do"], s["out"], g, self.status, ws)
+            if ev is not None:
+                ev["bwd"][i][0].record()
+            bd.bd_attn_bwd_main(s["do"], s["q"], s["k"], s["v"], s["lse"], s["seg"], g, self.status, ws,
+                                s["dk"], s["dv"])
+            if ev is not None:
+                ev["bwd"][i][1].record()
+            bd.bd_attn_bwd_finalize(g, self.status, ws, s["dq"])
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.config]
+    grad_dtype = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    ranks = None if args.shards is None else {int(x) for x in args.shards.split(",")}
+    rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks)
+    total_flop, fwd_flop, bwd_flop = rep.flops()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        rep.step()
+    torch.cuda.synchronize()
+    if int(rep.status.item()) != 0:
+        raise RuntimeError(f"device status {int(rep.status.item()):#x} after warm-up")
+
+    n = len(rep.shards)
+    ev_steps = [{"fwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
+                 "bwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]}
+                for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    smi_index = visible[local_rank].strip() if local_rank < len(visible) else str(local_rank)
+    with ClockSampler(smi_index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(args.steps):
+            rep.step(ev_steps[k])
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    if int(rep.status.item()) != 0:
+        raise RuntimeError(f"device status {int(rep.status.item()):#x} in the timed region")
+    ms = start.elapsed_time(stop)
+    fwd_ms = sum(e["fwd"][i][0].elapsed_time(e["fwd"][i][1]) for e in ev_steps for i in range(n))
+    bwd_ms = sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(rep, args, total_flop, world)
+
+    if rank != 0:
+        return None
+    peaks = read_peaks()
+    value = world * total_flop / (ms_per_step * 1e-3) / 1e12
+    bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    traffic = None
+    if TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha():
+        traffic = TRAFFIC["bytes_per_launch"]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.key}: {w.title}", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "S": w.S,
+                   "cp_size": w.cp_size, "L": w.L, "ranks": [s["r"] for s in rep.plan], "window": w.window, "kv": w.kv,
+                   "grad_dtype": args.grad_dtype, "l2": "inputs larger than L2 (K/V 268 MB), no flush",
+                   "pairs": sum(s["pairs"] for s in rep.shards), "seed": args.seed},
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
+        "fwd_tflops": round(fwd_flop * args.steps / (fwd_ms * 1e-3) / 1e12, 2),
+        "bwd_main_tflops": round(bwd_achieved, 2),
+        "roofline": {"kernel": "bwd_kernel (K4, backward main)", "bound": "tensor", "achieved": round(bwd_achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
+                     "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
+                     "traffic": traffic,
+                     "flops_per_launch": bwd_flop / len(rep.shards),
+                     "avg_launch_ms": round(bwd_ms / (args.steps * len(rep.shards)), 4)},
+        "gpu_launches": rep.launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    return line
+
+
+def run_e2e(rep: Replica, args, total_flop: float, world: int) -> dict:
+    """Same step through the C ABI with host buffers: pinned host inputs copied in
+    and every output copied back inside the timed region."""
+    dev = rep.dev
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+    h_doc = pin(rep.doc)
+    h_k, h_v = pin(rep.k_full), pin(rep.v_full)
+    h_in = [(pin(s["q"]), pin(s["do"])) for s in rep.shards]
+    h_out = [{n: torch.empty(s[n].shape, dtype=s[n].dtype, pin_memory=True) for n in ("out", "lse", "dq", "dk", "dv")}
+             for s in rep.shards]
+    full_kv = all(s["k"].data_ptr() == rep.k_full.data_ptr() for s in rep.shards)
+    h2d = h_doc.numel() * 4 + h_k.numel() * 2 + h_v.numel() * 2 + sum(a.numel() * 2 + b.numel() * 2 for a, b in h_in)
+    d2h = sum(sum(t.numel() * t.element_size() for t in o.values()) for o in h_out)
+
+    def step():
+        rep.doc.copy_(h_doc, non_blocking=True)
+        rep.k_full.copy_(h_k, non_blocking=True)
+        rep.v_full.copy_(h_v, non_blocking=True)
+        for s, (hq, hd) in zip(rep.shards, h_in):
+            s["q"].copy_(hq, non_blocking=True)
+            s["do"].copy_(hd, non_blocking=True)
+            if not full_kv:
+                a = s["g"].kv_offset
+                s["k"].copy_(rep.k_full[:, :, a:a + s["g"].S_kv])
+                s["v"].copy_(rep.v_full[:, :, a:a + s["g"].S_kv])
+        rep.step()
+        for s, o in zip(rep.shards, h_out):
+            for n, t in o.items():
+                t.copy_(s[n], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, args.steps // 2)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(world * total_flop / (ms * 1e-3) / 1e12, 2), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(w: synth.Workload, seed: int, n_heads: int = 4, rank_index: int = 3):
+    """fp64 oracle forward + backward on a bounded slice of the workload: batch row 0,
+    the first `n_heads` query heads of kv group 0, every local row of one shard."""
+    import oracle
+    doc = synth.doc_layout(w.layout, w.B, w.S, seed)
+    plan = shard_plan(w, doc)
+    sh = plan[min(rank_index, len(plan) - 1)]
+    k, v = synth.kv_rows(w, seed, sh["kv_offset"], sh["kv_offset"] + sh["S_kv"])
+    q = synth.q_shard(w, sh["r"], seed)[:1, :n_heads]
+    do = synth.dout_shard(w, sh["r"], seed)[:1, :n_heads]
+    g = oracle.geom(1, n_heads, 1, w.D, w.S, w.L, sh["row_offset"], sh["kv_offset"], sh["S_kv"], w.window)
+    args = (q, k[:1, :1], v[:1, :1], do, doc[:1], g)
+    flop = 14.0 * w.D * n_heads * pairs_closed_form(doc[:1], sh["row_offset"], w.L, w.window)
+    desc = (f"{w.key} shard r={sh['r']}: batch row 0, {n_heads} query heads of kv group 0, all {w.L} local rows, "
+            f"fwd + full bwd (dq, dk, dv)")
+    return args, flop, desc
+
+
+def time_oracle(args_tuple):
+    import oracle
+    q, k, v, do, doc, g = args_tuple
+    t0 = time.perf_counter()
+    oracle.fwd(q, k, v, doc, g)
+    oracle.bwd(q, k, v, do, doc, g)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    n = os.environ.get("OMP_NUM_THREADS")
+    if n and n.isdigit():
+        return int(n)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w: synth.Workload, seed: int, n_heads: int) -> dict:
+    args, flop, desc = oracle_sample(w, seed, n_heads=n_heads)
+    secs = time_oracle(args)
+    return {"value": round(flop / secs / 1e12, 6), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc, "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank: int, world: int):
+    """The oracle as the reference arm: each step is a bounded sample of the workload
+    on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.config]
+    sample_args, flop, desc = oracle_sample(w, args.seed, n_heads=1)
+    for _ in range(args.warmup):
+        time_oracle(sample_args)
+    secs = [time_oracle(sample_args) for _ in range(args.steps)]
+    ms = 1e3 * sum(secs) / len(secs)
+    value = flop / (ms * 1e-3) / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.key}: {w.title}", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "S": w.S,
+                       "cp_size": w.cp_size, "L": w.L, "window": w.window, "kv": w.kv, "seed": args.seed},
+            "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="C2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32")
+    ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-heads", type=int, default=4, help="query heads in the oracle's timed sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 must be launched with torchrun (one process per GPU)")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from sliding_window_attention_device_gb300 import build as _build
+    _build.build()
+    try:
+        line = run_ours(args, rank, world, local_rank)
+        if line is not None:
+            if world == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[args.config], args.seed, args.cpu_heads)
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -161,6 +161,21 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
                 const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
                 int32_t* status, bd_stream_t stream);
 
+/* The three stages bd_attn_bwd runs, one kernel each, for callers that want
+ * to schedule or time them separately (same arguments, same rules):
+ *  _prep:     delta[B,Hq,L] = rowsum(dout * out) in fp32 and a zeroed fp32 dq
+ *             accumulator, both in `workspace`;
+ *  _main:     dk, dv (written in full) and the dq accumulation in `workspace`;
+ *  _finalize: dq = scale * accumulator in grad_dtype.
+ * They must run in this order on one stream with the same workspace. */
+int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* g, void* workspace, int32_t* status,
+                     bd_stream_t stream);
+int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                     const void* seg, const bd_geom* g, int grad_dtype, void* dk, void* dv, void* workspace,
+                     int32_t* status, bd_stream_t stream);
+int bd_attn_bwd_finalize(const bd_geom* g, int grad_dtype, void* dq, void* workspace, int32_t* status,
+                         bd_stream_t stream);
+
 /* Human-readable text for a host return code. */
 const char* bd_attn_strerror(int code);
 

@@ -15,9 +15,13 @@ namespace bd {
 cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
-cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const int32_t* seg, const Geom& g, const void* dout, const void* out, const float* lse,
-                       void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st);
+cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
+                            cudaStream_t st);
+cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse, void* dk,
+                            void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st);
+cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
+                                cudaStream_t st);
 size_t bwd_workspace_bytes(const Geom& g);
 
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
@@ -106,6 +110,19 @@ int make_map(CUtensorMap* m, const void* ptr, int D, int rows, int planes, int b
   return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
 }
 
+// 3-D fp32 map over [planes][rows][D] with a (64 x 64 x 1) box and no swizzle:
+// the fp32 dq accumulator, target of the backward's bulk reduce-add.
+int make_map_f32(CUtensorMap* m, const void* ptr, int D, int rows, int planes) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(rows) * D * 4};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBwdQ), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
 }  // namespace
@@ -158,25 +175,65 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, co
                             static_cast<cudaStream_t>(stream)));
 }
 
+int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* gi, void* workspace, int32_t* status,
+                     bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!dout || !out || !workspace || !status) return BD_ERR_ARG;
+  if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_bwd_prep(g, dout, out, workspace, status, static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                     const void* seg, const bd_geom* gi, int grad_dtype, void* dk, void* dv, void* workspace,
+                     int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!dout || !q || !k || !v || !lse || !seg || !dk || !dv || !workspace || !status) return BD_ERR_ARG;
+  if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  if (!load_encode()) return BD_ERR_CUDA;
+  CUtensorMap mq, mdo, mk, mv, mdq;
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kBwdQ) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kBwdQ) ||
+      make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) || make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
+      make_map_f32(&mdq, workspace, g.D, g.L, g.B * g.Hq))
+    return BD_ERR_CUDA;
+  return cuda_rc(launch_bwd_main(mq, mdo, mk, mv, mdq, static_cast<const int32_t*>(seg), g, lse, dk, dv,
+                                 grad_dtype == BD_DTYPE_BF16, workspace, status, static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* workspace, int32_t* status,
+                         bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!dq || !workspace || !status) return BD_ERR_ARG;
+  if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
+  if (!aligned16(dq) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_bwd_finalize(g, dq, grad_dtype == BD_DTYPE_BF16, workspace, status,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,
                 const void* seg, const bd_geom* gi, int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
                 int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  // check everything up front so that a bad argument enqueues nothing
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return BD_ERR_ARG;
-  if (int rc = check_device()) return rc;
-  if (!load_encode()) return BD_ERR_CUDA;
-  CUtensorMap mq, mdo, mk, mv;
-  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kBwdQ) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kBwdQ) ||
-      make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) || make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile))
-    return BD_ERR_CUDA;
-  return cuda_rc(launch_bwd(mq, mdo, mk, mv, static_cast<const int32_t*>(seg), g, dout, out, lse, dq, dk, dv,
-                            grad_dtype == BD_DTYPE_BF16, workspace, status, static_cast<cudaStream_t>(stream)));
+  if (int rc = bd_attn_bwd_prep(dout, out, gi, workspace, status, stream)) return rc;
+  if (int rc = bd_attn_bwd_main(dout, q, k, v, lse, seg, gi, grad_dtype, dk, dv, workspace, status, stream))
+    return rc;
+  return bd_attn_bwd_finalize(gi, grad_dtype, dq, workspace, status, stream);
 }
 
 const char* bd_attn_strerror(int code) {

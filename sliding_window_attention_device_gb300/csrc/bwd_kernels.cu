@@ -98,6 +98,28 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }
 
 // ------------------------------------------------------------------ K4
+template <int D>
+struct BwdCfg {
+  static constexpr int kDp = D < 128 ? D : 128;  // dK / dV columns per pass
+  static constexpr int kPasses = D / kDp;
+  static constexpr int kNsq = D == 256 ? 1 : (D == 128 ? 3 : 4);  // Q / dO stages
+  // dQ^T is double-buffered in tensor memory: columns [128,192) and [192,256).
+  static constexpr uint32_t kColS = 0, kColDp = 64, kColDq = 128, kColDv = 256, kColDk = 384;
+  // For D <= 128 the dq partial tile is staged in shared memory (64 q x 64 d
+  // fp32 per slot) and added to the accumulator with TMA bulk reduce-add;
+  // D = 256 has no shared memory left and uses red.add.
+  static constexpr bool kTmaDq = D <= 128;
+  static constexpr int kDqChunks = kDp / 64;
+  static constexpr int kStageSlots = kTmaDq ? kDqChunks : 0;
+};
+
+template <int SLOTS>
+struct DqStage {
+  alignas(1024) float buf[SLOTS][kBwdQ * 64];
+};
+template <>
+struct DqStage<0> {};
+
 template <int D, int NSQ>
 struct BwdSmem {
   static constexpr int kChunks = D / 64;
@@ -110,30 +132,22 @@ struct BwdSmem {
   alignas(1024) uint8_t q[NSQ][kChunks][kQChunk];
   alignas(1024) uint8_t dout[NSQ][kChunks][kQChunk];
   alignas(1024) uint8_t ds[kKChunk];  // dS^T, 128 keys x 64 q, bf16, 128B-swizzled
-  float lse2[NSQ][kBwdQ];
-  float delta[NSQ][kBwdQ];
-  int jlo[NSQ][kBwdQ];
-  int jhi[NSQ][kBwdQ];
+  DqStage<BwdCfg<D>::kStageSlots> stage;
+  alignas(16) float lse2[NSQ][kBwdQ];  // per q row: lse * log2(e)
+  alignas(16) float delta[NSQ][kBwdQ];
+  int jlo[NSQ][kBwdQ];  // per q row: first allowed K/V buffer row
   uint64_t kv_full, q_full[NSQ], q_empty[NSQ];
-  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
+  uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
   int b, kt, q64_lo, nq64, n_real, skip;
 };
 
 template <int D>
-struct BwdCfg {
-  static constexpr int kDp = D < 128 ? D : 128;  // dK / dV columns per pass
-  static constexpr int kPasses = D / kDp;
-  static constexpr int kNsq = D == 256 ? 1 : (D == 128 ? 2 : 3);
-  static constexpr uint32_t kColS = 0, kColDp = 64, kColDq = 128, kColDv = 256, kColDk = 384;
-};
-
-template <int D>
 __global__ void __launch_bounds__(384, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-               const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
+               const __grid_constant__ CUtensorMap tm_dq, const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
                const float* __restrict__ delta, float* __restrict__ dq_acc, void* __restrict__ dk,
                void* __restrict__ dv, int grads_bf16, int32_t* status) {
   using Cfg = BwdCfg<D>;
@@ -141,7 +155,8 @@ __global__ void __launch_bounds__(384, 1)
   using Smem = BwdSmem<D, NSQ>;
   constexpr int kChunks = Smem::kChunks;
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw so the compiler keeps the shared address space
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hk = blockIdx.x % g.Hkv;
   volatile int* vstatus = status;
@@ -178,8 +193,10 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&s.p_full, 128);
     mbar_init(&s.ds_full, 128);
     mbar_init(&s.ds_empty, 1);
-    mbar_init(&s.dq_full, 1);
-    mbar_init(&s.dq_empty, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.dq_full[i], 1);
+      mbar_init(&s.dq_empty[i], 128);
+    }
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, 128);
     mbar_init(&s.mma_drain, 1);
@@ -263,25 +280,33 @@ __global__ void __launch_bounds__(384, 1)
     int issued = 0;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ, n = it / NSQ;
-      if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
       int pass, h, q0;
       decode(it, pass, h, q0);
-      for (int c = lane; c < kBwdQ; c += 32) {
-        const int i = q0 + c;
-        float l2 = 0.f, dl = 0.f;
-        int lo = 1, hi = 0;
+      // the per-row values are fetched before waiting for the free stage so
+      // that their global-load latency overlaps the wait
+      float l2[2], dl[2];
+      int lo[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = q0 + lane + 32 * e;
+        l2[e] = 0.f;
+        dl[e] = 0.f;
+        lo[e] = 0x7fffffff;  // padding / out-of-range rows attend nothing
         if (i < n_real) {
           const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
-          l2 = lse[row] * 1.4426950408889634f;
-          dl = delta[row];
+          l2[e] = lse[row] * 1.4426950408889634f;
+          dl[e] = delta[row];
           const int p = g.row_offset + i;
-          lo = row_lo_window(seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i], p, g.window) - g.kv_offset;
-          hi = p - g.kv_offset;
+          lo[e] = row_lo_window(seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i], p, g.window) - g.kv_offset;
         }
-        s.lse2[st][c] = l2;
-        s.delta[st][c] = dl;
-        s.jlo[st][c] = lo;
-        s.jhi[st][c] = hi;
+      }
+      if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = lane + 32 * e;
+        s.lse2[st][c] = l2[e];
+        s.delta[st][c] = dl[e];
+        s.jlo[st][c] = lo[e];
       }
       __syncwarp();
       if (lane == 0) {
@@ -343,12 +368,14 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t db = umma_desc_sw128(smem_u32(s.dout[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
           umma_ts(tbase + Cfg::kColDv, tbase + Cfg::kColS + ks * 8, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
         }
-        if (NSQ > 1 && it + 1 < n_it) {
-          const int st1 = (it + 1) % NSQ;
-          if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
+        // S^T of the next q tile goes in now only if its Q has already landed;
+        // otherwise it waits until dK / dQ of this tile have been issued.
+        bool s_next = false;
+        if (NSQ > 1 && it + 1 < n_it && mbar_test_wait(&s.q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) {
           tc_fence_after();
-          issue_st(Cfg::kColS, s.k, s.q[st1]);
+          issue_st(Cfg::kColS, s.k, s.q[(it + 1) % NSQ]);
           umma_commit(&s.s_full);
+          s_next = true;
         }
         // dK += dS^T Q[:, pass] ; dQ^T = K[:, pass]^T dS^T
         if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
@@ -359,21 +386,22 @@ __global__ void __launch_bounds__(384, 1)
           const uint64_t db = umma_desc_sw128(smem_u32(s.q[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
           umma_ss(tbase + Cfg::kColDk, da, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
         }
-        if (it > 0 && !wait(&s.dq_empty, (it - 1) & 1)) { ok = false; break; }
+        const int bq = it & 1;  // dQ^T tensor-memory buffer
+        if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kTile / 16; ++ks) {
           const uint64_t da = umma_desc_sw128(smem_u32(s.k[pass * (kDp / 64)]) + ks * 2048, Smem::kKChunk, 1024);
           const uint64_t db = umma_desc_sw128(smem_u32(s.ds) + ks * 2048, Smem::kKChunk, 1024);
-          umma_ss(tbase + Cfg::kColDq, da, db, idDQ, ks > 0 ? 1u : 0u);
+          umma_ss(tbase + Cfg::kColDq + 64 * bq, da, db, idDQ, ks > 0 ? 1u : 0u);
         }
-        umma_commit(&s.dq_full);
+        umma_commit(&s.dq_full[bq]);
         umma_commit(&s.ds_empty);
         umma_commit(&s.q_empty[st]);
         if (last_of_pass) umma_commit(&s.acc_full);
         if (it + 1 < n_it) {
           const int st1 = (it + 1) % NSQ;
-          if (NSQ == 1) {
+          if (!s_next) {  // also guarantees dO of the next tile for dP^T below
             if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
             tc_fence_after();
             issue_st(Cfg::kColS, s.k, s.q[st1]);
@@ -409,13 +437,33 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tbase + lane_off + Cfg::kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(tbase + lane_off + Cfg::kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
-      const bool all_real = q0 + kBwdQ - 1 < n_real;
-      const bool full = all_real && s.jlo[st][kBwdQ - 1] <= j && j <= s.jhi[st][0];
+      // The q columns this key row may pair with form one interval [c_lo, c_hi):
+      // key j <= row p  <=>  c >= j - (row_offset + q0 - kv_offset), and the
+      // rows' lower bounds lo(p) are non-decreasing, so lo(p) <= j holds on a
+      // prefix of the real rows (binary search over the stage's bounds).
+      const int c_real = min(kBwdQ, n_real - q0);
+      const int c_lo = max(0, j - (g.row_offset + q0 - g.kv_offset));
+      int c_hi = 0;
+      {
+        int a = 0, e = c_real;  // first c in [0, c_real) with jlo[c] > j
+        while (a < e) {
+          const int mid = (a + e) >> 1;
+          if (s.jlo[st][mid] > j) e = mid; else a = mid + 1;
+        }
+        c_hi = a;
+      }
       float p[64];
+      const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st]);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool allowed = full || (s.jlo[st][c] <= j && j <= s.jhi[st][c]);
-        p[c] = allowed ? fast_exp2(__uint_as_float(sr[c]) * sl2 - s.lse2[st][c]) : 0.f;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l = l4[c4];
+        const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          const float pe = fast_exp2(__uint_as_float(sr[c]) * sl2 - lv[e]);
+          p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+        }
       }
       uint32_t pk[32];
 #pragma unroll
@@ -430,11 +478,14 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tbase + lane_off + Cfg::kColDp, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
       tmem_ld32(tbase + lane_off + Cfg::kColDp + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_ld();
+      const float4* d4 = reinterpret_cast<const float4*>(s.delta[st]);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float d0 = p[2 * c] * (__uint_as_float(sr[2 * c]) - s.delta[st][2 * c]);
-        const float d1 = p[2 * c + 1] * (__uint_as_float(sr[2 * c + 1]) - s.delta[st][2 * c + 1]);
-        pk[c] = pack_bf16x2(d0, d1);
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 dl = d4[c4];
+        const int c = 4 * c4;
+        pk[2 * c4] = pack_bf16x2(p[c] * (__uint_as_float(sr[c]) - dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - dl.y));
+        pk[2 * c4 + 1] =
+            pack_bf16x2(p[c + 2] * (__uint_as_float(sr[c + 2]) - dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - dl.w));
       }
       if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       // 128 B row of dS^T in the 128B-swizzled K-major layout
@@ -483,28 +534,63 @@ __global__ void __launch_bounds__(384, 1)
     const int r = tid - 256;  // d index within the pass == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool active = (warp & 3) * 32 < kDp;  // D = 64: lanes 64..127 hold nothing useful
+    const bool issuer = tid == 256;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       int pass, h, q0;
       decode(it, pass, h, q0);
-      if (!warp_wait(&s.dq_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-      tc_fence_after();
+      const int bq = it & 1;
+      bool got = warp_wait(&s.dq_full[bq], (it >> 1) & 1, &s.abort_flag, vstatus);
       uint32_t qv[64];
-      if (active) {
-        tmem_ld32(tbase + lane_off + Cfg::kColDq, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
-        tmem_ld32(tbase + lane_off + Cfg::kColDq + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
-        tmem_wait_ld();
+      if (got) {
+        tc_fence_after();
+        if (active) {
+          const uint32_t col = Cfg::kColDq + 64 * bq;
+          tmem_ld32(tbase + lane_off + col, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+          tmem_ld32(tbase + lane_off + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+          tmem_wait_ld();
+        }
+        tc_fence_before();
+        mbar_arrive(&s.dq_empty[bq]);
       }
-      tc_fence_before();
-      mbar_arrive(&s.dq_empty);
-      if (active) {
-        float* base = dq_acc + ((static_cast<size_t>(b) * g.Hq + h) * g.L) * D + pass * kDp + r;
-        const int cmax = min(kBwdQ, n_real - q0);
+      if constexpr (Cfg::kTmaDq) {
+        // Stage this iteration's 64 x kDp tile in shared memory and add it to
+        // the accumulator with TMA bulk reduce-add. The previous iteration's
+        // reduce must have finished reading the slots first; the barrier also
+        // makes the abort decision uniform over the warpgroup.
+        if (issuer) bulk_wait_group_read<0>();
+        if (!named_bar_and(1, 128, got)) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          float* slot = s.stage.buf[r >> 6];
 #pragma unroll
-        for (int c = 0; c < kBwdQ; ++c)
-          if (c < cmax) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+          for (int c = 0; c < kBwdQ; ++c) slot[c * 64 + (r & 63)] = __uint_as_float(qv[c]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (issuer) {
+#pragma unroll
+          for (int ch = 0; ch < Cfg::kDqChunks; ++ch)
+            tma_reduce_add_3d(&tm_dq, s.stage.buf[ch], pass * kDp + ch * 64, q0, b * g.Hq + h);
+          bulk_commit_group();
+        }
+      } else {
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          float* base = dq_acc + ((static_cast<size_t>(b) * g.Hq + h) * g.L) * D + pass * kDp + r;
+          const int cmax = min(kBwdQ, n_real - q0);
+#pragma unroll
+          for (int c = 0; c < kBwdQ; ++c)
+            if (c < cmax) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+        }
       }
     }
+    if (Cfg::kTmaDq && issuer) bulk_wait_group<0>();
     if (!ok) {
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
@@ -522,60 +608,79 @@ __global__ void __launch_bounds__(384, 1)
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+unsigned grid_for(long long work_items) {
+  const long long blocks = (work_items + 255) / 256;
+  return static_cast<unsigned>(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
+}
+
 template <int D>
-cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
-                         const int32_t* seg, const Geom& g, const __nv_bfloat16* dout, const __nv_bfloat16* out,
-                         const float* lse, void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status,
-                         cudaStream_t st) {
-  const long long rows = static_cast<long long>(g.B) * g.Hq * g.L;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(static_cast<size_t>(rows) * D * 4));
-  {
-    const long long blocks = (rows * (D / 8) + 255) / 256;
-    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
-    bwd_pre_kernel<D><<<grid, 256, 0, st>>>(dout, out, delta, dq_acc, rows, status);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    const size_t smem = sizeof(BwdSmem<D, BwdCfg<D>::kNsq>) + 1024;  // + 1 KB to align the swizzled tiles
-    auto kern = bwd_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
-    if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kern<<<static_cast<unsigned>(grid), 384, smem, st>>>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16,
-                                                         status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    const long long n = rows * D;
-    const long long blocks = (n / 8 + 255) / 256;
-    const unsigned grid = static_cast<unsigned>(blocks < 152 * 16 ? blocks : 152 * 16);
-    dq_convert_kernel<<<grid, 256, 0, st>>>(dq_acc, dq, n, g.scale, bf16, status);
-  }
+cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse,
+                          const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
+                          cudaStream_t st) {
+  const size_t smem = sizeof(BwdSmem<D, BwdCfg<D>::kNsq>) + 1024;  // + 1 KB to align the swizzled tiles
+  auto kern = bwd_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), 384, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv,
+                                                       bf16, status);
   return cudaGetLastError();
 }
 }  // namespace
 
+// Workspace: fp32 dq accumulator [B,Hq,L,D], then fp32 delta [B,Hq,L].
 size_t bwd_workspace_bytes(const Geom& g) {
   const size_t rows = static_cast<size_t>(g.B) * g.Hq * g.L;
   return align256(rows * g.D * 4) + align256(rows * 4);
 }
 
-// K4a (delta, zero the dq accumulator) -> K4 (dK, dV, dq accumulation) -> K4b (dq).
-cudaError_t launch_bwd(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
-                       const int32_t* seg, const Geom& g, const void* dout, const void* out, const float* lse,
-                       void* dq, void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
+static float* ws_delta(const Geom& g, void* workspace) {
+  const size_t rows = static_cast<size_t>(g.B) * g.Hq * g.L;
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * g.D * 4));
+}
+
+// K4a: delta and a zeroed dq accumulator.
+cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
+                            cudaStream_t st) {
+  const long long rows = static_cast<long long>(g.B) * g.Hq * g.L;
   const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
   const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(out);
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = ws_delta(g, workspace);
+  const unsigned grid = grid_for(rows * (g.D / 8));
   switch (g.D) {
-    case 64: return launch_bwd_d<64>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
-    case 128: return launch_bwd_d<128>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
-    case 256: return launch_bwd_d<256>(mq, mdo, mk, mv, seg, g, dob, ob, lse, dq, dk, dv, bf16, workspace, status, st);
+    case 64: bwd_pre_kernel<64><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
+    case 128: bwd_pre_kernel<128><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
+    case 256: bwd_pre_kernel<256><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
     default: return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+// K4: dK, dV and the dq accumulation. `mdq` maps the fp32 accumulator at the
+// start of `workspace` as [B*Hq][L][D] with 64 x 64 boxes.
+cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse, void* dk,
+                            void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
+  float* dq_acc = static_cast<float*>(workspace);
+  const float* delta = ws_delta(g, workspace);
+  switch (g.D) {
+    case 64: return launch_main_d<64>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 128: return launch_main_d<128>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 256: return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// K4b: dq = scale * accumulator.
+cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
+                                cudaStream_t st) {
+  const long long n = static_cast<long long>(g.B) * g.Hq * g.L * g.D;
+  dq_convert_kernel<<<grid_for(n / 8), 256, 0, st>>>(static_cast<const float*>(workspace), dq, n, g.scale, bf16,
+                                                     status);
+  return cudaGetLastError();
 }
 
 }  // namespace bd

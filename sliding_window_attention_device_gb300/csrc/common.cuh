@@ -2,7 +2,7 @@
 #pragma once
 
 #include <cstdint>
-#include "../../include/bdattn.h"
+#include "bdattn.h"  // include/ is on the include path
 
 namespace bd {
 

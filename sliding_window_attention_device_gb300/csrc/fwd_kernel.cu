@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
   using TM = FwdTmem<D, NQ>;
   constexpr int kChunks = Smem::kChunks;
   extern __shared__ uint8_t smem_raw[];
-  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from smem_raw so the compiler keeps the shared address space
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_pairs = g.Hq / NQ;
   const int pair = blockIdx.x % n_pairs;
