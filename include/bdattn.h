@@ -176,6 +176,30 @@ int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void*
 int bd_attn_bwd_finalize(const bd_geom* g, int grad_dtype, void* dq, void* workspace, int32_t* status,
                          bd_stream_t stream);
 
+/* Allocation-free backward. Same arguments and results as bd_attn_bwd
+ * except that there is no `workspace`: the dq accumulator and delta live in
+ * one scratch array that the library places in device memory at load time
+ * (BD_NOALLOC_SCRATCH_BYTES per GPU, held until the process exits). It is for
+ * callers that can hand the library their inputs and outputs but cannot
+ * allocate device memory at call time -- for example a host that reserved
+ * its whole memory budget up front, or a plugin whose framework forbids
+ * allocations outside its own allocator -- so it calls no cudaMalloc,
+ * cudaFree or allocating routine. The paper pages have no counterpart; this
+ * is a deployment convenience.
+ *  - Returns BD_ERR_SCRATCH_TOO_SMALL (nothing enqueued) when
+ *    bd_attn_bwd_workspace_bytes(g) exceeds BD_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on each device looks up the scratch array's device
+ *    address (cudaGetSymbolAddress, with that device current); make that
+ *    first call before any stream capture.
+ *  - Every call on a device shares the one array, and each call starts by
+ *    zeroing the part it accumulates into. Calls whose kernels overlap on the
+ *    GPU (other streams, other host threads) race on it: serialise them. */
+#define BD_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define BD_ERR_SCRATCH_TOO_SMALL 4
+int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk,
+                        void* dv, int32_t* status, bd_stream_t stream);
+
 /* Human-readable text for a host return code. */
 const char* bd_attn_strerror(int code);
 

@@ -33,7 +33,7 @@ REGIONS = ("hdr", "cu_q", "cu_k", "row_lo", "qt_krange", "kt_qrange", "full_bits
 
 EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_fwd",
            "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
-           "bd_attn_bwd_finalize", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
+           "bd_attn_bwd_finalize", "bd_attn_bwd_noalloc", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
 
 
 class Geom(ctypes.Structure):

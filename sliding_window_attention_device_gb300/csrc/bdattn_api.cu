@@ -236,12 +236,59 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
   return bd_attn_bwd_finalize(gi, grad_dtype, dq, workspace, status, stream);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------- allocation-free backward
+// The backward's scratch (fp32 dq accumulator + delta) for callers that cannot
+// allocate device memory at call time: one array per GPU, reserved when the
+// library is loaded and shared by every bd_attn_bwd_noalloc call on that GPU.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[BD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device. Looked up once
+// per device (with that device current); host code must never hand the
+// symbol itself to a kernel, it is only a host-side stand-in.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return BD_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                        const float* lse, const void* seg, const bd_geom* gi, int grad_dtype, void* dq, void* dk,
+                        void* dv, int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (bwd_workspace_bytes(g) > BD_NOALLOC_SCRATCH_BYTES) return BD_ERR_SCRATCH_TOO_SMALL;
+  if (int rc = check_device()) return rc;
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(&scratch)) return rc;
+  // same three stages as bd_attn_bwd; the prep stage zeroes the accumulator
+  return bd_attn_bwd(dout, q, k, v, out, lse, seg, gi, grad_dtype, dq, dk, dv, scratch, status, stream);
+}
+
 const char* bd_attn_strerror(int code) {
   switch (code) {
     case BD_OK: return "ok";
     case BD_ERR_ARG: return "invalid argument (nothing enqueued)";
     case BD_ERR_CUDA: return "CUDA runtime or driver call failed";
     case BD_ERR_UNSUPPORTED: return "device is not a Blackwell sm_10x GPU";
+    case BD_ERR_SCRATCH_TOO_SMALL:
+      return "problem needs more backward scratch than bd_attn_bwd_noalloc's static 16 MiB (use bd_attn_bwd)";
     default: return "unknown bdattn error code";
   }
 }

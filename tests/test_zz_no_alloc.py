@@ -1,0 +1,77 @@
+"""The allocation-free backward, bd_attn_bwd_noalloc, called through the C ABI.
+
+Some callers can give the library their input and output buffers but cannot
+allocate device memory while they run (a host that reserved its whole memory
+budget at start-up, a plugin whose framework allows only its own allocator).
+This entry point keeps the backward's scratch in a static per-GPU array
+instead of a caller workspace. Its results must match bd_attn_bwd's within the
+parity tolerance, on consecutive calls that reuse the same scratch, and a
+problem larger than the scratch must be refused with a clear error.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import MAX_ABS, MEAN_ABS, make_case
+from sliding_window_attention_device_gb300 import bdattn, synth
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_TOO_SMALL = 4
+
+
+def _noalloc():
+    lib = bdattn.load()
+    f = lib.bd_attn_bwd_noalloc
+    P = ctypes.c_void_p
+    f.argtypes = [P, P, P, P, P, P, P, ctypes.POINTER(bdattn.Geom), ctypes.c_int, P, P, P, P, P]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _close(name, got, ref):
+    d = (got.double() - ref.double()).abs()
+    assert torch.isfinite(got).all(), name
+    assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS, \
+        f"{name}: max {d.max().item():.3e} mean {d.mean().item():.3e}"
+
+
+def test_noalloc_matches_bwd_on_consecutive_calls():
+    w = synth.Workload("N", "noalloc", B=2, Hq=4, Hkv=2, D=128, S=1280, cp_size=4,
+                       layout=("uniform", 20, 300, 40), window=0)
+    c = make_case(w, 2, seed=3)
+    dev = torch.device("cuda")
+    g = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], w.window)
+    assert bdattn.bwd_workspace_bytes(g) <= (16 << 20)
+    doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    seg, status = bdattn.bd_attn_seg_build(doc, g)
+    out, lse = bdattn.bd_attn_fwd(q, k, v, seg, g, status)
+    ref = bdattn.bd_attn_bwd(do, q, k, v, out, lse, seg, g, status)
+    f = _noalloc()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call in range(2):
+        dq = torch.full_like(ref[0], float("nan"))
+        dk = torch.full_like(ref[1], float("nan"))
+        dv = torch.full_like(ref[2], float("nan"))
+        rc = f(P(do), P(q), P(k), P(v), P(out), P(lse), P(seg), ctypes.byref(g), bdattn.BD_DTYPE_F32, P(dq), P(dk),
+               P(dv), P(status), stream)
+        assert rc == 0, bdattn.strerror(rc)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for name, got, r in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+            _close(f"call {call} {name}", got, r)
+
+
+def test_noalloc_refuses_problems_larger_than_its_scratch():
+    g = bdattn.geom(2, 32, 8, 128, 32768, 4096, 0, 0, 32768)  # needs ~135 MB of scratch
+    assert bdattn.bwd_workspace_bytes(g) > (16 << 20)
+    f = _noalloc()
+    P = ctypes.c_void_p
+    rc = f(P(16), P(16), P(16), P(16), P(16), P(16), P(16), ctypes.byref(g), bdattn.BD_DTYPE_F32, P(16), P(16),
+           P(16), P(16), None)
+    assert rc == SCRATCH_TOO_SMALL
+    assert "16 MiB" in bdattn.strerror(rc)
