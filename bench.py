@@ -360,19 +360,24 @@ def run_e2e(rep: Replica, args, total_flop: float, world: int) -> dict:
 # ------------------------------------------------------------ CPU oracle
 def oracle_sample(w: synth.Workload, seed: int, n_heads: int = 4, rank_index: int = 3):
     """fp64 oracle forward + backward on a bounded slice of the workload: batch row 0,
-    the first `n_heads` query heads of kv group 0, every local row of one shard."""
+    the first `n_heads` query heads (whole GQA groups when n_heads >= Hq/Hkv), every
+    local row of one shard."""
     import oracle
     doc = synth.doc_layout(w.layout, w.B, w.S, seed)
     plan = shard_plan(w, doc)
     sh = plan[min(rank_index, len(plan) - 1)]
+    n_heads = max(1, min(n_heads, w.Hq))
+    n_kv = 1 if n_heads <= w.G else -(-n_heads // w.G)
+    if n_heads > w.G:
+        n_heads = n_kv * w.G
     k, v = synth.kv_rows(w, seed, sh["kv_offset"], sh["kv_offset"] + sh["S_kv"])
     q = synth.q_shard(w, sh["r"], seed)[:1, :n_heads]
     do = synth.dout_shard(w, sh["r"], seed)[:1, :n_heads]
-    g = oracle.geom(1, n_heads, 1, w.D, w.S, w.L, sh["row_offset"], sh["kv_offset"], sh["S_kv"], w.window)
-    args = (q, k[:1, :1], v[:1, :1], do, doc[:1], g)
+    g = oracle.geom(1, n_heads, n_kv, w.D, w.S, w.L, sh["row_offset"], sh["kv_offset"], sh["S_kv"], w.window)
+    args = (q, k[:1, :n_kv], v[:1, :n_kv], do, doc[:1], g)
     flop = 14.0 * w.D * n_heads * pairs_closed_form(doc[:1], sh["row_offset"], w.L, w.window)
-    desc = (f"{w.key} shard r={sh['r']}: batch row 0, {n_heads} query heads of kv group 0, all {w.L} local rows, "
-            f"fwd + full bwd (dq, dk, dv)")
+    desc = (f"{w.key} shard r={sh['r']}: batch row 0, query heads 0..{n_heads - 1} ({n_kv} kv groups), "
+            f"all {w.L} local rows, fwd + full bwd (dq, dk, dv)")
     return args, flop, desc
 
 
@@ -436,7 +441,8 @@ def main():
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-heads", type=int, default=4, help="query heads in the oracle's timed sample")
+    ap.add_argument("--cpu-heads", type=int, default=32,
+                    help="query heads of batch row 0 in the oracle's timed CPU-baseline slice")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
