@@ -25,7 +25,8 @@
 // because 2 x 256 fp32 columns would fill the whole tensor memory.
 //   warp 0  loads (TMA for K, V, Q, dO; the q rows' lse / delta / mask bounds)
 //   warp 1  issues the MMAs          warp 2  owns the tensor memory
-//   warps 4-7  P, dS (thread = key row)      warps 8-11  dQ read-out
+//   warps 4-7 and 12-15  P, dS (thread = key row; q columns 0-31 / 32-63)
+//   warps 8-11  dQ read-out (thread = d row)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -143,13 +144,15 @@ struct BwdSmem {
   int b, kt, q64_lo, nq64, n_real, skip;
 };
 
+constexpr int kBwdThreads = 512;
+
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-               const __grid_constant__ CUtensorMap tm_dq, const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
-               const float* __restrict__ delta, float* __restrict__ dq_acc, void* __restrict__ dk,
-               void* __restrict__ dv, int grads_bf16, int32_t* status) {
+               const __grid_constant__ CUtensorMap tm_dq, const int32_t* __restrict__ seg, const Geom g,
+               const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dq_acc,
+               void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
   using Cfg = BwdCfg<D>;
   constexpr int NSQ = Cfg::kNsq, kDp = Cfg::kDp, kPasses = Cfg::kPasses;
   using Smem = BwdSmem<D, NSQ>;
@@ -190,15 +193,15 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&s.s_full, 1);
     mbar_init(&s.dp_full, 1);
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.ds_full, 128);
+    mbar_init(&s.p_full, 256);
+    mbar_init(&s.ds_full, 256);
     mbar_init(&s.ds_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.dq_full[i], 1);
       mbar_init(&s.dq_empty[i], 128);
     }
     mbar_init(&s.acc_full, 1);
-    mbar_init(&s.acc_empty, 128);
+    mbar_init(&s.acc_empty, 256);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
   }
@@ -209,6 +212,9 @@ __global__ void __launch_bounds__(384, 1)
   const int n_it_pass = G * nq64;
   const int n_it = kPasses * n_it_pass;
   const size_t kv_row0 = (static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv;
+  // P / dS warpgroups: warps 4-7 (half 0, q columns 0-31) and 12-15 (half 1, 32-63)
+  const bool is_pds = (warp >= 4 && warp < 8) || warp >= 12;
+  const int half = warp >= 12 ? 1 : 0;
 
   auto store_row = [&](void* base, size_t elem_off, const float* vals32) {
     if (grads_bf16) {
@@ -231,14 +237,15 @@ __global__ void __launch_bounds__(384, 1)
   };
 
   if (n_it == 0) {
-    // No query attends this K/V tile: its dK / dV rows are zero.
-    if (warp >= 4 && warp < 8) {
-      const int j = kt * kTile + (tid - 128);
+    // No query attends this K/V tile: its dK / dV rows are zero (each half
+    // warpgroup writes half of the columns).
+    if (is_pds) {
+      const int j = kt * kTile + (warp & 3) * 32 + lane;
       if (j < g.S_kv) {
         float z[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) z[e] = 0.f;
-        for (int c = 0; c < D; c += 32) {
+        for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
           store_row(dk, (kv_row0 + j) * D + c, z);
           store_row(dv, (kv_row0 + j) * D + c, z);
         }
@@ -333,24 +340,28 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idST = idesc_bf16(128, kBwdQ, false, false);
       constexpr uint32_t idDKV = idesc_bf16(128, kDp, false, true);
       constexpr uint32_t idDQ = idesc_bf16(128, kBwdQ, true, true);
-      auto issue_st = [&](uint32_t col, uint8_t (*a)[Smem::kKChunk], uint8_t (*bq)[Smem::kQChunk]) {
+      const uint64_t dK_major = umma_desc_sw128(0, 16, 1024);              // K-major operands
+      const uint64_t dMN_q = umma_desc_sw128(0, Smem::kQChunk, 1024);      // MN-major, 64-row chunks
+      const uint64_t dMN_k = umma_desc_sw128(0, Smem::kKChunk, 1024);      // MN-major, 128-row chunks
+      const uint32_t a_k = smem_u32(s.k[0]), a_v = smem_u32(s.v[0]), a_ds = smem_u32(s.ds);
+      const uint32_t a_q = smem_u32(s.q[0][0]), a_do = smem_u32(s.dout[0][0]);
+      constexpr uint32_t kQStage = kChunks * Smem::kQChunk;
+      auto issue_st = [&](uint32_t col, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int ch = ks >> 2, kk = ks & 3;
-          const uint64_t da = umma_desc_sw128(smem_u32(a[ch]) + kk * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(smem_u32(bq[ch]) + kk * 32, 16, 1024);
-          umma_ss(tbase + col, da, db, idST, ks > 0 ? 1u : 0u);
+          const uint32_t off_a = (ks >> 2) * Smem::kKChunk + (ks & 3) * 32;
+          const uint32_t off_b = (ks >> 2) * Smem::kQChunk + (ks & 3) * 32;
+          umma_ss(tbase + col, desc_at(dK_major, a_base + off_a), desc_at(dK_major, b_base + off_b), idST,
+                  ks > 0 ? 1u : 0u);
         }
       };
-      auto wait = [&](uint64_t* bar, uint32_t par) {
-        return pipe_wait(bar, par, &s.abort_flag, vstatus);
-      };
+      auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
       bool ok = wait(&s.kv_full, 0) && wait(&s.q_full[0], 0);
       if (ok) {
         tc_fence_after();
-        issue_st(Cfg::kColS, s.k, s.q[0]);
+        issue_st(Cfg::kColS, a_k, a_q);
         umma_commit(&s.s_full);
-        issue_st(Cfg::kColDp, s.v, s.dout[0]);
+        issue_st(Cfg::kColDp, a_v, a_do);
         umma_commit(&s.dp_full);
       }
       for (int it = 0; ok && it < n_it; ++it) {
@@ -359,21 +370,24 @@ __global__ void __launch_bounds__(384, 1)
         decode(it, pass, h, q0);
         const bool first_of_pass = (it % n_it_pass) == 0;
         const bool last_of_pass = (it % n_it_pass) == n_it_pass - 1;
+        const uint32_t pass_off_q = st * kQStage + pass * (kDp / 64) * Smem::kQChunk;
         if (first_of_pass && pass > 0 && !wait(&s.acc_empty, (pass - 1) & 1)) { ok = false; break; }
-        // dV += P^T dO[:, pass]
+        // dV += P^T dO[:, pass]; P^T is bf16 in tensor memory, q columns 0-31 at
+        // column offset 0 and 32-63 at offset 48 (each half writes over its own S^T)
         if (!wait(&s.p_full, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < kBwdQ / 16; ++ks) {
-          const uint64_t db = umma_desc_sw128(smem_u32(s.dout[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
-          umma_ts(tbase + Cfg::kColDv, tbase + Cfg::kColS + ks * 8, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
+          const uint32_t a_col = Cfg::kColS + (ks < 2 ? ks * 8 : 48 + (ks - 2) * 8);
+          umma_ts(tbase + Cfg::kColDv, tbase + a_col, desc_at(dMN_q, a_do + pass_off_q + ks * 2048), idDKV,
+                  (!first_of_pass || ks > 0) ? 1u : 0u);
         }
         // S^T of the next q tile goes in now only if its Q has already landed;
         // otherwise it waits until dK / dQ of this tile have been issued.
         bool s_next = false;
         if (NSQ > 1 && it + 1 < n_it && mbar_test_wait(&s.q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) {
           tc_fence_after();
-          issue_st(Cfg::kColS, s.k, s.q[(it + 1) % NSQ]);
+          issue_st(Cfg::kColS, a_k, a_q + ((it + 1) % NSQ) * kQStage);
           umma_commit(&s.s_full);
           s_next = true;
         }
@@ -381,20 +395,17 @@ __global__ void __launch_bounds__(384, 1)
         if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kBwdQ / 16; ++ks) {
-          const uint64_t da = umma_desc_sw128(smem_u32(s.ds) + ks * 32, 16, 1024);
-          const uint64_t db = umma_desc_sw128(smem_u32(s.q[st][pass * (kDp / 64)]) + ks * 2048, Smem::kQChunk, 1024);
-          umma_ss(tbase + Cfg::kColDk, da, db, idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kBwdQ / 16; ++ks)
+          umma_ss(tbase + Cfg::kColDk, desc_at(dK_major, a_ds + ks * 32), desc_at(dMN_q, a_q + pass_off_q + ks * 2048),
+                  idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
         const int bq = it & 1;  // dQ^T tensor-memory buffer
         if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t a_kpass = a_k + pass * (kDp / 64) * Smem::kKChunk;
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks) {
-          const uint64_t da = umma_desc_sw128(smem_u32(s.k[pass * (kDp / 64)]) + ks * 2048, Smem::kKChunk, 1024);
-          const uint64_t db = umma_desc_sw128(smem_u32(s.ds) + ks * 2048, Smem::kKChunk, 1024);
-          umma_ss(tbase + Cfg::kColDq + 64 * bq, da, db, idDQ, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kTile / 16; ++ks)
+          umma_ss(tbase + Cfg::kColDq + 64 * bq, desc_at(dMN_k, a_kpass + ks * 2048), desc_at(dMN_k, a_ds + ks * 2048),
+                  idDQ, ks > 0 ? 1u : 0u);
         umma_commit(&s.dq_full[bq]);
         umma_commit(&s.ds_empty);
         umma_commit(&s.q_empty[st]);
@@ -404,10 +415,10 @@ __global__ void __launch_bounds__(384, 1)
           if (!s_next) {  // also guarantees dO of the next tile for dP^T below
             if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
             tc_fence_after();
-            issue_st(Cfg::kColS, s.k, s.q[st1]);
+            issue_st(Cfg::kColS, a_k, a_q + st1 * kQStage);
             umma_commit(&s.s_full);
           }
-          issue_st(Cfg::kColDp, s.v, s.dout[st1]);
+          issue_st(Cfg::kColDp, a_v, a_do + st1 * kQStage);
           umma_commit(&s.dp_full);
         }
       }
@@ -418,11 +429,12 @@ __global__ void __launch_bounds__(384, 1)
       umma_commit(&s.mma_drain);
       mbar_wait_drain(&s.mma_drain, 0);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------ P and dS (key rows)
-    const int r = tid - 128;
+  } else if (is_pds) {
+    // ---------------------------- P and dS (key rows; one half of the q columns)
+    const int r = (warp & 3) * 32 + lane;  // key row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int j = kt * kTile + r;  // K/V buffer row of this thread
+    const int c0 = half * 32;      // first q column of this half
     const float sl2 = g.scale * 1.4426950408889634f;
     uint8_t* ds_row = s.ds + r * 128;
     bool ok = true;
@@ -433,29 +445,28 @@ __global__ void __launch_bounds__(384, 1)
       if (!warp_wait(&s.q_full[st], (it / NSQ) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       if (!warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[64];
-      tmem_ld32(tbase + lane_off + Cfg::kColS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tbase + lane_off + Cfg::kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      uint32_t sr[32];
+      tmem_ld32(tbase + lane_off + Cfg::kColS + c0, sr);
       tmem_wait_ld();
       // The q columns this key row may pair with form one interval [c_lo, c_hi):
       // key j <= row p  <=>  c >= j - (row_offset + q0 - kv_offset), and the
       // rows' lower bounds lo(p) are non-decreasing, so lo(p) <= j holds on a
       // prefix of the real rows (binary search over the stage's bounds).
       const int c_real = min(kBwdQ, n_real - q0);
-      const int c_lo = max(0, j - (g.row_offset + q0 - g.kv_offset));
-      int c_hi = 0;
+      const int c_lo = max(0, j - (g.row_offset + q0 - g.kv_offset)) - c0;
+      int c_hi;
       {
         int a = 0, e = c_real;  // first c in [0, c_real) with jlo[c] > j
         while (a < e) {
           const int mid = (a + e) >> 1;
           if (s.jlo[st][mid] > j) e = mid; else a = mid + 1;
         }
-        c_hi = a;
+        c_hi = a - c0;
       }
-      float p[64];
-      const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st]);
+      float p[32];
+      const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st] + c0);
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int c4 = 0; c4 < 8; ++c4) {
         const float4 l = l4[c4];
         const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
@@ -465,22 +476,21 @@ __global__ void __launch_bounds__(384, 1)
           p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
         }
       }
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
-      tmem_st32(tbase + lane_off + Cfg::kColS, pk);
+      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      tmem_st16(tbase + lane_off + Cfg::kColS + 48 * half, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.p_full);
 
       if (!warp_wait(&s.dp_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld32(tbase + lane_off + Cfg::kColDp, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tbase + lane_off + Cfg::kColDp + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tbase + lane_off + Cfg::kColDp + c0, sr);
       tmem_wait_ld();
-      const float4* d4 = reinterpret_cast<const float4*>(s.delta[st]);
+      const float4* d4 = reinterpret_cast<const float4*>(s.delta[st] + c0);
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
+      for (int c4 = 0; c4 < 8; ++c4) {
         const float4 dl = d4[c4];
         const int c = 4 * c4;
         pk[2 * c4] = pack_bf16x2(p[c] * (__uint_as_float(sr[c]) - dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - dl.y));
@@ -488,10 +498,11 @@ __global__ void __launch_bounds__(384, 1)
             pack_bf16x2(p[c + 2] * (__uint_as_float(sr[c + 2]) - dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - dl.w));
       }
       if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-      // 128 B row of dS^T in the 128B-swizzled K-major layout
+      // this half's 64 B of the key row of dS^T, 128B-swizzled K-major layout
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) {
-        uint4 w = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int c16 = 4 * half + k4;
+        const uint4 w = make_uint4(pk[4 * k4], pk[4 * k4 + 1], pk[4 * k4 + 2], pk[4 * k4 + 3]);
         *reinterpret_cast<uint4*>(ds_row + ((c16 ^ (r & 7)) << 4)) = w;
       }
       fence_proxy_async_smem();
@@ -499,11 +510,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(&s.ds_full);
 
       if ((it % n_it_pass) == n_it_pass - 1) {
-        // end of a pass: write this thread's dK / dV row (columns of the pass)
+        // end of a pass: write this thread's dK / dV row (its half of the pass's columns)
         if (!warp_wait(&s.acc_full, pass & 1, &s.abort_flag, vstatus)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < kDp; c += 32) {
+        for (int c = half * (kDp / 2); c < (half + 1) * (kDp / 2); c += 32) {
           uint32_t vv[32];
           float f[32];
           tmem_ld32(tbase + lane_off + Cfg::kColDv + c, vv);
@@ -529,7 +540,7 @@ __global__ void __launch_bounds__(384, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the pass == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -624,7 +635,7 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), 384, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv,
+  kern<<<static_cast<unsigned>(grid), kBwdThreads, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv,
                                                        bf16, status);
   return cudaGetLastError();
 }

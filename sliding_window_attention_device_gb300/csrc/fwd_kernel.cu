@@ -173,23 +173,25 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     // ----------------------------------------------------------- MMA issuer
     constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
     constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+    const uint64_t dK_major = umma_desc_sw128(0, 16, 1024);                 // Q, K: K-major
+    const uint64_t dMN = umma_desc_sw128(0, Smem::kChunkBytes, 1024);       // V: MN-major
+    const uint32_t a_q = smem_u32(s.q[0][0]), a_k = smem_u32(s.k[0][0]), a_v = smem_u32(s.v[0][0]);
+    constexpr uint32_t kTileBytes = kChunks * Smem::kChunkBytes;
     auto issue_s = [&](int qi, int st) {
       const uint32_t d = tbase + TM::kS(qi);
+      const uint32_t qa = a_q + qi * kTileBytes, ka = a_k + st * kTileBytes;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        const int ch = ks >> 2, kk = ks & 3;
-        const uint64_t a = umma_desc_sw128(smem_u32(s.q[qi][ch]) + kk * 32, 16, 1024);
-        const uint64_t bb = umma_desc_sw128(smem_u32(s.k[st][ch]) + kk * 32, 16, 1024);
-        umma_ss(d, a, bb, idS, ks > 0 ? 1u : 0u);
+        const uint32_t off = (ks >> 2) * Smem::kChunkBytes + (ks & 3) * 32;
+        umma_ss(d, desc_at(dK_major, qa + off), desc_at(dK_major, ka + off), idS, ks > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int qi, int st, bool acc) {
       const uint32_t d = tbase + TM::kO(qi);
+      const uint32_t va = a_v + st * kTileBytes;
 #pragma unroll
-      for (int ks = 0; ks < kTile / 16; ++ks) {
-        const uint64_t bb = umma_desc_sw128(smem_u32(s.v[st][0]) + ks * 2048, Smem::kChunkBytes, 1024);
-        umma_ts(d, tbase + TM::kS(qi) + ks * 8, bb, idPV, (acc || ks > 0) ? 1u : 0u);
-      }
+      for (int ks = 0; ks < kTile / 16; ++ks)
+        umma_ts(d, tbase + TM::kS(qi) + ks * 8, desc_at(dMN, va + ks * 2048), idPV, (acc || ks > 0) ? 1u : 0u);
     };
     bool ok = pipe_wait(&s.q_full, 0, &s.abort_flag, vstatus) &&
               pipe_wait(&s.k_full[0], 0, &s.abort_flag, vstatus);

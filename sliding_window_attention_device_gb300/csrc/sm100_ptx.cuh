@@ -249,6 +249,12 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr, uint32_t
   return d;
 }
 
+// Descriptor `base` (built for address 0) moved to `smem_addr`: only the
+// 14-bit start-address field differs between tiles of one operand kind.
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t smem_addr) {
+  return base | static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                    // D format: f32
