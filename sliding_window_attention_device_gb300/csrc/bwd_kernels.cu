@@ -136,7 +136,6 @@ struct BwdSmem {
   DqStage<BwdCfg<D>::kStageSlots> stage;
   alignas(16) float lse2[NSQ][kBwdQ];  // per q row: lse * log2(e)
   alignas(16) float delta[NSQ][kBwdQ];
-  int jlo[NSQ][kBwdQ];  // per q row: first allowed K/V buffer row
   uint64_t kv_full, q_full[NSQ], q_empty[NSQ];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
@@ -292,19 +291,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the per-row values are fetched before waiting for the free stage so
       // that their global-load latency overlaps the wait
       float l2[2], dl[2];
-      int lo[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int i = q0 + lane + 32 * e;
         l2[e] = 0.f;
         dl[e] = 0.f;
-        lo[e] = 0x7fffffff;  // padding / out-of-range rows attend nothing
         if (i < n_real) {
           const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
           l2[e] = lse[row] * 1.4426950408889634f;
           dl[e] = delta[row];
-          const int p = g.row_offset + i;
-          lo[e] = row_lo_window(seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i], p, g.window) - g.kv_offset;
         }
       }
       if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
@@ -313,7 +308,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int c = lane + 32 * e;
         s.lse2[st][c] = l2[e];
         s.delta[st][c] = dl[e];
-        s.jlo[st][c] = lo[e];
       }
       __syncwarp();
       if (lane == 0) {
@@ -437,6 +431,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int c0 = half * 32;      // first q column of this half
     const float sl2 = g.scale * 1.4426950408889634f;
     uint8_t* ds_row = s.ds + r * 128;
+    // A real row p >= key s attends s iff p lies in the document that contains
+    // s (documents are contiguous runs) and, with a window, p - s < W. So the
+    // rows attending s are [s, min(doc_end(s), s + W)) intersected with the
+    // real rows. doc_end(s) is fixed for the CTA: find it once from cu_q.
+    const int key = g.kv_offset + j;  // global position of this thread's key
+    int doc_end = -0x40000000;        // keys no local row attends
+    {
+      const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+      const int32_t* cu_q = seg + g.off[BD_SEG_OFF_CU_Q] + b * (g.L + 1);
+      const int n_seg = hdr[BD_SEG_N_SEG];
+      if (n_seg > 0 && key >= hdr[BD_SEG_S_FIRST] && key < hdr[BD_SEG_REAL_END]) {
+        int k = 0;  // segment containing key: the last k with row_offset + cu_q[k] <= key
+        if (key >= g.row_offset) {
+          int a = 0, e = n_seg - 1;
+          while (a < e) {
+            const int mid = (a + e + 1) >> 1;
+            if (g.row_offset + cu_q[mid] <= key) a = mid; else e = mid - 1;
+          }
+          k = a;
+        }
+        doc_end = g.row_offset + cu_q[k + 1];
+      }
+    }
+    const int win_end = g.window > 0 ? key + g.window : 0x3fffffff;
+    const int row_end = min(doc_end, win_end);  // rows [key, row_end) attend this key
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSQ;
@@ -448,21 +467,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t sr[32];
       tmem_ld32(tbase + lane_off + Cfg::kColS + c0, sr);
       tmem_wait_ld();
-      // The q columns this key row may pair with form one interval [c_lo, c_hi):
-      // key j <= row p  <=>  c >= j - (row_offset + q0 - kv_offset), and the
-      // rows' lower bounds lo(p) are non-decreasing, so lo(p) <= j holds on a
-      // prefix of the real rows (binary search over the stage's bounds).
-      const int c_real = min(kBwdQ, n_real - q0);
-      const int c_lo = max(0, j - (g.row_offset + q0 - g.kv_offset)) - c0;
-      int c_hi;
-      {
-        int a = 0, e = c_real;  // first c in [0, c_real) with jlo[c] > j
-        while (a < e) {
-          const int mid = (a + e) >> 1;
-          if (s.jlo[st][mid] > j) e = mid; else a = mid + 1;
-        }
-        c_hi = a - c0;
-      }
+      // q columns [c_lo, c_hi) of this tile attend the key (relative to c0)
+      const int row0 = g.row_offset + q0;
+      const int c_lo = max(0, key - row0) - c0;
+      const int c_hi = min(min(kBwdQ, n_real - q0), row_end - row0) - c0;
       float p[32];
       const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st] + c0);
 #pragma unroll
