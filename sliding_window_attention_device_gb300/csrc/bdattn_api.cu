@@ -23,6 +23,7 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st);
 size_t bwd_workspace_bytes(const Geom& g);
+int bwd_q_box_rows(int D);
 
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
   __shared__ uint64_t bar;
@@ -198,7 +199,8 @@ int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void*
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
   CUtensorMap mq, mdo, mk, mv, mdq;
-  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kBwdQ) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kBwdQ) ||
+  const int qbox = bwd_q_box_rows(g.D);
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, qbox) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, qbox) ||
       make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) || make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
       make_map_f32(&mdq, workspace, g.D, g.L, g.B * g.Hq))
     return BD_ERR_CUDA;

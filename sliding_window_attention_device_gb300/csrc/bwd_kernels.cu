@@ -678,6 +678,14 @@ cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, vo
   return cudaGetLastError();
 }
 
+cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
+                               cudaStream_t st);
+
+// Rows of the q / dout TMA boxes the backward main kernel for this head dim expects.
+int bwd_q_box_rows(int D) { return D <= 128 ? 128 : kBwdQ; }
+
 // K4: dK, dV and the dq accumulation. `mdq` maps the fp32 accumulator at the
 // start of `workspace` as [B*Hq][L][D] with 64 x 64 boxes.
 cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
@@ -686,8 +694,9 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
   float* dq_acc = static_cast<float*>(workspace);
   const float* delta = ws_delta(g, workspace);
   switch (g.D) {
-    case 64: return launch_main_d<64>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
-    case 128: return launch_main_d<128>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 64:
+    case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
+      return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 256: return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
