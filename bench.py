@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the backward main
 # kernel, from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (see
 # profiles/), valid only for the kernel source with this sha256 prefix.
-TRAFFIC = {"kernel": "bwd_kernel<128>", "source_sha256": None, "bytes_per_launch": None}
+TRAFFIC = {"kernel": "bwd128_kernel<128>", "source_sha256": None, "bytes_per_launch": None}
 
 
 # ------------------------------------------------------------------ workload
@@ -159,8 +159,11 @@ class ClockSampler:
 
 
 def kernel_source_sha() -> str:
-    p = os.path.join(ROOT, "sliding_window_attention_device_gb300", "csrc", "bwd_kernels.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the sources the D = 128 backward main kernel is built from."""
+    h = hashlib.sha256()
+    for f in ("bwd128_kernel.cu", "common.cuh", "pipeline.cuh", "sm100_ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "sliding_window_attention_device_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------- our path
@@ -194,7 +197,9 @@ class Replica:
             ws = max(ws, bdattn.bwd_workspace_bytes(g))
             self.shards.append(d)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
-        self.launches_per_step = 6 * len(self.shards)
+        # per shard: segment build + classification, forward, backward prep,
+        # zero-fill of unattended dK / dV + backward main, dq finalize
+        self.launches_per_step = 7 * len(self.shards)
 
     def flops(self) -> tuple[float, float, float]:
         D, Hq = self.w.D, self.w.Hq
@@ -294,7 +299,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
-        "roofline": {"kernel": "bwd_kernel (K4, backward main)", "bound": "tensor", "achieved": round(bwd_achieved, 2),
+        "roofline": {"kernel": "bwd128_kernel<128> (backward main stage, with its dK/dV zero-fill launch)", "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
                      "traffic": traffic,

@@ -111,7 +111,9 @@ typedef struct {
 #define BD_SEG_OFF_FULL_BITS 6  /* [B][nqt][nkw] bit kt set: tile (qt, kt) is entirely allowed */
 #define BD_SEG_OFF_FWD_WORK 7   /* [B*nqt]       q tiles (b*nqt+qt), most K/V tiles first */
 #define BD_SEG_OFF_BWD_WORK 8   /* [B*nkt]       K/V tiles (b*nkt+kt), most q rows first */
-#define BD_SEG_OFF_COUNTS 9     /* [8]           0: full tiles, 1: partial tiles, 2: empty tiles */
+#define BD_SEG_OFF_COUNTS 9     /* [8]           0: full tiles, 1: partial tiles, 2: empty tiles,
+                                                 3: K/V tiles some local row attends (the first
+                                                    entries of the backward work list) */
 #define BD_SEG_OFF_TOTAL 10     /* total words */
 #define BD_SEG_NOFF 11
 

@@ -293,5 +293,5 @@ def read_seg(seg: torch.Tensor, g: Geom) -> dict:
     return {"rows": rows,
             "fwd_work": a[lay["fwd_work"]: lay["fwd_work"] + B * nqt].copy(),
             "bwd_work": a[lay["bwd_work"]: lay["bwd_work"] + B * nkt].copy(),
-            "counts": a[lay["counts"]: lay["counts"] + 3].copy(),
+            "counts": a[lay["counts"]: lay["counts"] + 4].copy(),
             "layout": lay}

@@ -52,8 +52,12 @@ struct Ctl {
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int b, kt, q_lo, nq, n_real, skip;
+  int b, kt, q_lo, nq, n_real, skip, mode;
 };
+
+// What a CTA does, from its position in the backward work list.
+constexpr int kModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
+constexpr int kModeWork = 1;  // an attended K/V tile
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
@@ -94,8 +98,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hk = blockIdx.x % g.Hkv;
   volatile int* vstatus = status;
 
+  const int item = blockIdx.x / g.Hkv;
   if (tid == 0) {
-    const int item = blockIdx.x / g.Hkv;
+    // the attended K/V tiles lead the work list; the grid must cover them
+    const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
+    int mode = kModeIdle;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv)
+      atomicOr(status, BD_STATUS_BOUNDS);
+    else
+      mode = item < n_att ? kModeWork : kModeIdle;
+    s.mode = mode;
+  }
+  __syncthreads();
+  if (s.mode != kModeWork) return;
+
+  if (tid == 0) {
     const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
     int ok = wi >= 0 && wi < g.B * g.nkt;
     const int b = ok ? wi / g.nkt : 0, kt = ok ? wi % g.nkt : 0;
@@ -106,7 +123,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_real = hdr[BD_SEG_N_REAL];
     const int32_t* qr = seg + g.off[BD_SEG_OFF_KT_QRANGE] + (b * g.nkt + kt) * 2;
     const int qlo = qr[0], qhi = qr[1];
-    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real;
+    // an attended tile has a non-empty q range
+    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real && qlo < qhi;
     if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
     s.b = b;
     s.kt = kt;
@@ -157,23 +175,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         p[e] = make_float4(vals32[4 * e + 0], vals32[4 * e + 1], vals32[4 * e + 2], vals32[4 * e + 3]);
     }
   };
-
-  if (n_it == 0) {
-    // No query attends this K/V tile: its dK / dV rows are zero.
-    if (is_pds) {
-      const int j = kt * kTile + (warp & 3) * 32 + lane;
-      if (j < g.S_kv) {
-        float z[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = 0.f;
-        for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
-          store_row(dk, (kv_row0 + j) * D + c, z);
-          store_row(dv, (kv_row0 + j) * D + c, z);
-        }
-      }
-    }
-    return;
-  }
 
   if (warp == 2) {
     tmem_alloc(&s.tmem_base, 512);
@@ -526,7 +527,10 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   auto kern = bwd128_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
+  // only tiles some local row can reach by position get a working CTA; with
+  // none reachable, B CTAs per kv head still zero dK / dV
+  const int reach = kv_tiles_reachable(g);
+  const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16,
                                                             status);

@@ -140,10 +140,13 @@ struct BwdSmem {
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int b, kt, q64_lo, nq64, n_real, skip;
+  int b, kt, q64_lo, nq64, n_real, skip, mode;
 };
 
 constexpr int kBwdThreads = 512;
+// What a backward CTA does, from its position in the work list.
+constexpr int kBwdModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
+constexpr int kBwdModeWork = 1;  // an attended K/V tile
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -163,8 +166,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int hk = blockIdx.x % g.Hkv;
   volatile int* vstatus = status;
 
+  const int item = blockIdx.x / g.Hkv;
   if (tid == 0) {
-    const int item = blockIdx.x / g.Hkv;
+    // the attended K/V tiles lead the work list; the grid must cover them
+    const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
+    int mode = kBwdModeIdle;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv)
+      atomicOr(status, BD_STATUS_BOUNDS);
+    else
+      mode = item < n_att ? kBwdModeWork : kBwdModeIdle;
+    s.mode = mode;
+  }
+  __syncthreads();
+  if (s.mode != kBwdModeWork) return;
+
+  if (tid == 0) {
     const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
     int ok = wi >= 0 && wi < g.B * g.nkt;
     const int b = ok ? wi / g.nkt : 0, kt = ok ? wi % g.nkt : 0;
@@ -175,7 +191,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int n_real = hdr[BD_SEG_N_REAL];
     const int32_t* qr = seg + g.off[BD_SEG_OFF_KT_QRANGE] + (b * g.nkt + kt) * 2;
     const int qlo = qr[0], qhi = qr[1];
-    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real;
+    // an attended tile has a non-empty q range
+    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real && qlo < qhi;
     const int nq64 = qhi > qlo ? (qhi - 1) / kBwdQ - qlo / kBwdQ + 1 : 0;
     if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
     s.b = b;
@@ -234,24 +251,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         p[e] = make_float4(vals32[4 * e + 0], vals32[4 * e + 1], vals32[4 * e + 2], vals32[4 * e + 3]);
     }
   };
-
-  if (n_it == 0) {
-    // No query attends this K/V tile: its dK / dV rows are zero (each half
-    // warpgroup writes half of the columns).
-    if (is_pds) {
-      const int j = kt * kTile + (warp & 3) * 32 + lane;
-      if (j < g.S_kv) {
-        float z[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = 0.f;
-        for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
-          store_row(dk, (kv_row0 + j) * D + c, z);
-          store_row(dv, (kv_row0 + j) * D + c, z);
-        }
-      }
-    }
-    return;
-  }
 
   if (warp == 2) {
     tmem_alloc(&s.tmem_base, 512);
@@ -627,6 +626,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// dK / dV of the K/V tiles no local row attends are zero; the attention
+// kernels' CTAs for those tiles exit at once and this streaming kernel writes
+// the zeros (every (tile, kv head) pair past the attended ones in the work list).
+__global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const int32_t* __restrict__ seg, const Geom g, void* dk,
+                                                          void* dv, int grads_bf16, int32_t* status) {
+  const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
+  if (n_att < 0 || n_att > g.B * g.nkt) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, BD_STATUS_BOUNDS);
+    return;
+  }
+  zero_unattended_kv(seg, g, n_att, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                     static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x), dk, dv, grads_bf16, status);
+}
+
 unsigned grid_for(long long work_items) {
   const long long blocks = (work_items + 255) / 256;
   return static_cast<unsigned>(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
@@ -641,7 +654,10 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
   auto kern = bwd_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const long long grid = static_cast<long long>(g.B) * g.nkt * g.Hkv;
+  // only tiles some local row can reach by position get a working CTA; with
+  // none reachable, B CTAs per kv head still zero dK / dV
+  const int reach = kv_tiles_reachable(g);
+  const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(grid), kBwdThreads, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv,
                                                        bf16, status);
@@ -693,6 +709,13 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
                             void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
   float* dq_acc = static_cast<float*>(workspace);
   const float* delta = ws_delta(g, workspace);
+  {
+    const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
+    const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
+    bwd_zero_kv_kernel<<<grid, 256, 0, st>>>(seg, g, dk, dv, bf16, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   switch (g.D) {
     case 64:
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes

@@ -53,4 +53,49 @@ __device__ __forceinline__ int row_lo_window(int doc_start, int p, int window) {
   return (window > 0 && p - window + 1 > doc_start) ? p - window + 1 : doc_start;
 }
 
+// Number of 128-row K/V tiles some local row can attend by position alone:
+// a row p in [row_offset, row_offset + L) attends keys s <= p and, with a
+// window W, s > p - W. Every tile the segment table marks as attended lies in
+// this range, so a backward grid of B x this many tiles covers them all.
+__host__ __device__ inline int kv_tiles_reachable(const Geom& g) {
+  const long long hi = static_cast<long long>(g.row_offset) + g.L - 1 - g.kv_offset;
+  const long long lo = g.window > 0 ? static_cast<long long>(g.row_offset) - g.window + 1 - g.kv_offset : 0;
+  const long long a = lo > 0 ? lo : 0;
+  const long long e = hi < g.S_kv - 1 ? hi : static_cast<long long>(g.S_kv) - 1;
+  return e < a ? 0 : static_cast<int>(e / kTile - a / kTile + 1);
+}
+
+#ifdef __CUDACC__
+// Zero dK / dV rows of the K/V tiles no local row attends. The backward work
+// list holds the n_att attended tiles first; the (position, kv head) pairs of
+// the rest, x = (z - n_att) * Hkv + hk, are taken by writer w of n_w as
+// x = w, w + n_w, ...; threads t = 0..nthr-1 share each tile. The stores are
+// marked streaming (evict-first) as nothing reads these lines again soon.
+__device__ inline void zero_unattended_kv(const int32_t* seg, const Geom& g, int n_att, int w, int n_w, int t, int nthr,
+                                          void* dk, void* dv, int grads_bf16, int32_t* status) {
+  const int n_items = g.B * g.nkt;
+  const long long n_pairs = static_cast<long long>(n_items - n_att) * g.Hkv;
+  const size_t row_bytes = static_cast<size_t>(g.D) * (grads_bf16 ? 2 : 4);  // a multiple of 16
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (long long x = w; x < n_pairs; x += n_w) {
+    const int z = n_att + static_cast<int>(x / g.Hkv), hk = static_cast<int>(x % g.Hkv);
+    const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + z];
+    if (wi < 0 || wi >= n_items) {
+      if (t == 0) atomicOr(status, BD_STATUS_BOUNDS);
+      continue;
+    }
+    const int b = wi / g.nkt, r0 = (wi % g.nkt) * kTile;
+    const int r1 = r0 + kTile < g.S_kv ? r0 + kTile : g.S_kv;
+    const size_t off = ((static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv + r0) * row_bytes;
+    const size_t n16 = static_cast<size_t>(r1 - r0) * row_bytes / 16;
+    uint4* pk = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dk) + off);
+    uint4* pv = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dv) + off);
+    for (size_t i = t; i < n16; i += nthr) {
+      __stcs(pk + i, zero);
+      __stcs(pv + i, zero);
+    }
+  }
+}
+#endif
+
 }  // namespace bd

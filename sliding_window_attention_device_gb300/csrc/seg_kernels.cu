@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(1024) classify_kernel(Geom g, int32_t* __restr
   __shared__ int s_red[32];
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int ro = g.row_offset, L = g.L, W = g.window;
-  int n_full = 0, n_part = 0;
+  int n_full = 0, n_part = 0, n_kv_att = 0;
 
   for (int b = 0; b < g.B; ++b) {
     const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
@@ -291,16 +291,19 @@ __global__ void __launch_bounds__(1024) classify_kernel(Geom g, int32_t* __restr
       const int i_end = a;
       kq[2 * kt] = (i_begin < i_end) ? i_begin : 0;
       kq[2 * kt + 1] = (i_begin < i_end) ? i_end : 0;
+      n_kv_att += i_begin < i_end ? 1 : 0;
     }
   }
   n_full = block_reduce(n_full, AddOp(), s_red);
   n_part = block_reduce(n_part, AddOp(), s_red);
+  n_kv_att = block_reduce(n_kv_att, AddOp(), s_red);
   if (tid == 0) {
     int32_t* counts = seg + g.off[BD_SEG_OFF_COUNTS];
     counts[0] = n_full;
     counts[1] = n_part;
     counts[2] = g.B * g.nqt * g.nkt - n_full - n_part;
-    for (int x = 3; x < 8; ++x) counts[x] = 0;
+    counts[3] = n_kv_att;  // these K/V tiles lead the backward work list
+    for (int x = 4; x < 8; ++x) counts[x] = 0;
   }
   __syncthreads();  // ranges written above are read below by other threads
 

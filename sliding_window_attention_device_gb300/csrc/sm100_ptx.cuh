@@ -312,4 +312,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
 
+// ------------------------------------------------- register redistribution
+// Executed by all threads of a warpgroup (128 consecutive threads). The
+// block's register pool is fixed at launch (threads x registers per thread);
+// an increase waits until other warpgroups have released enough registers, so
+// the per-warpgroup targets must sum to at most the launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void wg_reg_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void wg_reg_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 }  // namespace bd

@@ -52,10 +52,18 @@ def run_gpu(c: dict, grad_dtype=torch.float32, bwd: bool = True) -> dict:
     doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
     q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
     seg, status = bdattn.bd_attn_seg_build(doc, g)
-    out, lse = bdattn.bd_attn_fwd(q, k, v, seg, g, status)
+    w = c["w"]
+    out = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((w.B, w.Hq, w.L), float("nan"), dtype=torch.float32, device=dev)
+    out, lse = bdattn.bd_attn_fwd(q, k, v, seg, g, status, out=out, lse=lse)
     res = dict(g=g, seg=seg, status=status, out=out, lse=lse)
     if bwd:
-        dq, dk, dv = bdattn.bd_attn_bwd(do, q, k, v, out, lse, seg, g, status, grad_dtype=grad_dtype)
+        # NaN-filled outputs: an element the kernels leave unwritten fails the finiteness checks
+        dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=grad_dtype, device=dev)
+        dk = torch.full((w.B, w.Hkv, c["S_kv"], w.D), float("nan"), dtype=grad_dtype, device=dev)
+        dv = torch.full_like(dk, float("nan"))
+        dq, dk, dv = bdattn.bd_attn_bwd(do, q, k, v, out, lse, seg, g, status, grad_dtype=grad_dtype,
+                                        dq=dq, dk=dk, dv=dv)
         res.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     res["status_word"] = int(status.item())

@@ -145,6 +145,7 @@ def test_tile_classification(seed, window, cp, kvmode):
         tab = _check_segments(doc, B, S, L, ro, kvo, skv, window)
         cls, m = _brute_tiles(doc, B, S, L, ro, kvo, skv, window)
         nqt, nkt = cls.shape[1:]
+        attended = set()  # K/V tiles (b * nkt + kt) some local row attends
         for b in range(B):
             row = tab["rows"][b]
             for qt in range(nqt):
@@ -163,9 +164,13 @@ def test_tile_classification(seed, window, cp, kvmode):
                 if rows.size == 0:
                     assert a == e == 0
                 else:
+                    attended.add(b * nkt + kt)
                     assert (a, e) == (rows[0], rows[-1] + 1) and rows.size == e - a, (b, kt, a, e, rows)
         n_full, n_part = int((cls == 2).sum()), int((cls == 1).sum())
-        assert tuple(tab["counts"]) == (n_full, n_part, cls.size - n_full - n_part)
+        assert tuple(tab["counts"][:3]) == (n_full, n_part, cls.size - n_full - n_part)
+        # the attended K/V tiles are counted and lead the backward work list
+        assert int(tab["counts"][3]) == len(attended)
+        assert set(tab["bwd_work"][:len(attended)].tolist()) == attended
         # work lists: permutations ordered by decreasing work
         fw = tab["fwd_work"]
         assert sorted(fw.tolist()) == list(range(B * nqt))
