@@ -199,8 +199,9 @@ class Replica:
             self.shards.append(d)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
         # per shard: segment build + classification, forward, backward prep,
-        # zero-fill of unattended dK / dV + backward main, dq finalize
-        self.launches_per_step = 7 * len(self.shards)
+        # zero-fill of unattended dK / dV + backward main, and (bf16 gradients
+        # only) the dq finalize; fp32 dq is accumulated in place
+        self.launches_per_step = (6 if grad_dtype == torch.float32 else 7) * len(self.shards)
 
     def flops(self) -> tuple[float, float, float]:
         D, Hq = self.w.D, self.w.Hq
@@ -219,14 +220,23 @@ class Replica:
         bd.bd_attn_fwd(s["q"], s["k"], s["v"], s["seg"], g, self.status, out=s["out"], lse=s["lse"])
         if ev is not None:
             ev["fwd"][i][1].record()
-        bd.bd_attn_bwd_prep(s["do"], s["out"], g, self.status, ws)
+        direct = s["dq"].dtype == torch.float32  # fp32 dq is its own accumulator: no finalize
+        if direct:
+            bd.bd_attn_bwd_prep_dq(s["do"], s["out"], g, self.status, ws, s["dq"])
+        else:
+            bd.bd_attn_bwd_prep(s["do"], s["out"], g, self.status, ws)
         if ev is not None:
             ev["bwd"][i][0].record()
-        bd.bd_attn_bwd_main(s["do"], s["q"], s["k"], s["v"], s["lse"], s["seg"], g, self.status, ws,
-                            s["dk"], s["dv"])
+        if direct:
+            bd.bd_attn_bwd_main_dq(s["do"], s["q"], s["k"], s["v"], s["lse"], s["seg"], g, self.status, ws,
+                                   s["dq"], s["dk"], s["dv"])
+        else:
+            bd.bd_attn_bwd_main(s["do"], s["q"], s["k"], s["v"], s["lse"], s["seg"], g, self.status, ws,
+                                s["dk"], s["dv"])
         if ev is not None:
             ev["bwd"][i][1].record()
-        bd.bd_attn_bwd_finalize(g, self.status, ws, s["dq"])
+        if not direct:
+            bd.bd_attn_bwd_finalize(g, self.status, ws, s["dq"])
 
     def step(self, ev=None):
         for i in range(len(self.shards)):

@@ -167,8 +167,9 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
  * to schedule or time them separately (same arguments, same rules):
  *  _prep:     delta[B,Hq,L] = rowsum(dout * out) in fp32 and a zeroed fp32 dq
  *             accumulator, both in `workspace`;
- *  _main:     dk, dv (written in full) and the dq accumulation in `workspace`;
- *  _finalize: dq = scale * accumulator in grad_dtype.
+ *  _main:     dk, dv (written in full) and the dq accumulation (of the final,
+ *             scaled gradient) in `workspace`;
+ *  _finalize: dq = accumulator, converted to grad_dtype.
  * They must run in this order on one stream with the same workspace. */
 int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* g, void* workspace, int32_t* status,
                      bd_stream_t stream);
@@ -177,6 +178,23 @@ int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void*
                      int32_t* status, bd_stream_t stream);
 int bd_attn_bwd_finalize(const bd_geom* g, int grad_dtype, void* dq, void* workspace, int32_t* status,
                          bd_stream_t stream);
+
+/* The same backward with the fp32 dq output as its own accumulator, in two
+ * stages and without a finalize pass (bd_attn_bwd takes this path when
+ * grad_dtype is BD_DTYPE_F32):
+ *  _prep_dq: delta in `workspace` (whose accumulator part is not used) and
+ *            dq [B,Hq,L,D] fp32 set to zero;
+ *  _main_dq: dk, dv in grad_dtype as bd_attn_bwd_main, and dq += scale * dS K
+ *            for every attended tile, so dq holds the final gradient when the
+ *            kernel ends.
+ * dq must be 16-byte aligned fp32 device memory (BD_ERR_ARG otherwise, or for
+ * a null dq); run _prep_dq then _main_dq on one stream with the same dq and
+ * workspace. */
+int bd_attn_bwd_prep_dq(const void* dout, const void* out, const bd_geom* g, void* workspace, float* dq,
+                        int32_t* status, bd_stream_t stream);
+int bd_attn_bwd_main_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                        const void* seg, const bd_geom* g, int grad_dtype, float* dq, void* dk, void* dv,
+                        void* workspace, int32_t* status, bd_stream_t stream);
 
 /* Allocation-free backward. Same arguments and results as bd_attn_bwd
  * except that there is no `workspace`: the dq accumulator and delta live in

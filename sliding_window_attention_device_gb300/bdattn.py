@@ -33,7 +33,8 @@ REGIONS = ("hdr", "cu_q", "cu_k", "row_lo", "qt_krange", "kt_qrange", "full_bits
 
 EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_fwd",
            "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
-           "bd_attn_bwd_finalize", "bd_attn_bwd_noalloc", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
+           "bd_attn_bwd_finalize", "bd_attn_bwd_prep_dq", "bd_attn_bwd_main_dq",
+           "bd_attn_bwd_noalloc", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
 
 
 class Geom(ctypes.Structure):
@@ -87,6 +88,10 @@ def load() -> ctypes.CDLL:
         lib.bd_attn_bwd_main.restype = ctypes.c_int
         lib.bd_attn_bwd_finalize.argtypes = [G, ctypes.c_int, P, P, P, P]
         lib.bd_attn_bwd_finalize.restype = ctypes.c_int
+        lib.bd_attn_bwd_prep_dq.argtypes = [P, P, G, P, P, P, P]
+        lib.bd_attn_bwd_prep_dq.restype = ctypes.c_int
+        lib.bd_attn_bwd_main_dq.argtypes = [P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
+        lib.bd_attn_bwd_main_dq.restype = ctypes.c_int
         lib.bd_attn_strerror.argtypes = [ctypes.c_int]
         lib.bd_attn_strerror.restype = ctypes.c_char_p
         lib.bd_attn_selftest_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
@@ -253,7 +258,7 @@ def bd_attn_bwd_main(dout, q, k, v, lse, seg, g: Geom, status, workspace, dk, dv
 
 
 def bd_attn_bwd_finalize(g: Geom, status, workspace, dq, stream=None):
-    """Stage 3 of bd_attn_bwd: dq = scale * accumulator, in the dtype of dq."""
+    """Stage 3 of bd_attn_bwd: dq = the (already scaled) accumulator, in the dtype of dq."""
     dev = dq.device
     if dq.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("dq must be float32 or bfloat16")
@@ -263,6 +268,41 @@ def bd_attn_bwd_finalize(g: Geom, status, workspace, dq, stream=None):
     code = BD_DTYPE_BF16 if dq.dtype == torch.bfloat16 else BD_DTYPE_F32
     _check(load().bd_attn_bwd_finalize(ctypes.byref(g), code, _ptr(dq), _ptr(workspace), _ptr(status),
                                        _stream(stream)), "bd_attn_bwd_finalize")
+
+
+def bd_attn_bwd_prep_dq(dout, out, g: Geom, status, workspace, dq, stream=None):
+    """Stage 1 with the fp32 dq as accumulator: delta in `workspace`, dq zeroed."""
+    dev = out.device
+    _need(dout, "dout", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    _need(out, "out", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
+    _need(dq, "dq", torch.float32, (g.B, g.Hq, g.L, g.D), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    _check(load().bd_attn_bwd_prep_dq(_ptr(dout), _ptr(out), ctypes.byref(g), _ptr(workspace), _ptr(dq),
+                                      _ptr(status), _stream(stream)), "bd_attn_bwd_prep_dq")
+
+
+def bd_attn_bwd_main_dq(dout, q, k, v, lse, seg, g: Geom, status, workspace, dq, dk, dv, stream=None):
+    """Stage 2 with the fp32 dq as accumulator: dk, dv (dtype of dk) and dq += scale * dS K."""
+    dev = q.device
+    gd = dk.dtype
+    if gd not in (torch.float32, torch.bfloat16):
+        raise ValueError("dk / dv must be float32 or bfloat16")
+    for name, t in (("dout", dout), ("q", q)):
+        _need(t, name, torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
+    _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
+    _need(dq, "dq", torch.float32, (g.B, g.Hq, g.L, g.D), dev)
+    _need(dk, "dk", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(dv, "dv", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    code = BD_DTYPE_BF16 if gd == torch.bfloat16 else BD_DTYPE_F32
+    _check(load().bd_attn_bwd_main_dq(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(seg), ctypes.byref(g),
+                                      code, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _ptr(status),
+                                      _stream(stream)), "bd_attn_bwd_main_dq")
 
 
 def selftest_wait_timeout(limit_ns: int, status: torch.Tensor, stream=None):

@@ -15,11 +15,11 @@ namespace bd {
 cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
-cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
-                            cudaStream_t st);
+cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
+                            int32_t* status, cudaStream_t st);
 cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse, void* dk,
-                            void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st);
+                            void* dv, int bf16, void* workspace, float* dq_f32, int32_t* status, cudaStream_t st);
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st);
 size_t bwd_workspace_bytes(const Geom& g);
@@ -176,19 +176,25 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, co
                             static_cast<cudaStream_t>(stream)));
 }
 
-int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* gi, void* workspace, int32_t* status,
-                     bd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// The prep and main stages with the dq accumulator either in the workspace
+// (dq_f32 == nullptr) or in the caller's fp32 dq buffer.
+int bwd_prep_impl(const void* dout, const void* out, const bd_geom* gi, void* workspace, float* dq_f32,
+                  int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
   if (!dout || !out || !workspace || !status) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
+  if (dq_f32 && !aligned16(dq_f32)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
-  return cuda_rc(launch_bwd_prep(g, dout, out, workspace, status, static_cast<cudaStream_t>(stream)));
+  return cuda_rc(launch_bwd_prep(g, dout, out, workspace, dq_f32, status, static_cast<cudaStream_t>(stream)));
 }
 
-int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void* v, const float* lse,
-                     const void* seg, const bd_geom* gi, int grad_dtype, void* dk, void* dv, void* workspace,
-                     int32_t* status, bd_stream_t stream) {
+int bwd_main_impl(const void* dout, const void* q, const void* k, const void* v, const float* lse, const void* seg,
+                  const bd_geom* gi, int grad_dtype, void* dk, void* dv, void* workspace, float* dq_f32,
+                  int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
   if (!dout || !q || !k || !v || !lse || !seg || !dk || !dv || !workspace || !status) return BD_ERR_ARG;
@@ -196,6 +202,7 @@ int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void*
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) ||
       !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return BD_ERR_ARG;
+  if (dq_f32 && !aligned16(dq_f32)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
   CUtensorMap mq, mdo, mk, mv, mdq;
@@ -205,7 +212,35 @@ int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void*
       make_map_f32(&mdq, workspace, g.D, g.L, g.B * g.Hq))
     return BD_ERR_CUDA;
   return cuda_rc(launch_bwd_main(mq, mdo, mk, mv, mdq, static_cast<const int32_t*>(seg), g, lse, dk, dv,
-                                 grad_dtype == BD_DTYPE_BF16, workspace, status, static_cast<cudaStream_t>(stream)));
+                                 grad_dtype == BD_DTYPE_BF16, workspace, dq_f32, status,
+                                 static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* gi, void* workspace, int32_t* status,
+                     bd_stream_t stream) {
+  return bwd_prep_impl(dout, out, gi, workspace, nullptr, status, stream);
+}
+
+int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                     const void* seg, const bd_geom* gi, int grad_dtype, void* dk, void* dv, void* workspace,
+                     int32_t* status, bd_stream_t stream) {
+  return bwd_main_impl(dout, q, k, v, lse, seg, gi, grad_dtype, dk, dv, workspace, nullptr, status, stream);
+}
+
+int bd_attn_bwd_prep_dq(const void* dout, const void* out, const bd_geom* gi, void* workspace, float* dq,
+                        int32_t* status, bd_stream_t stream) {
+  if (!dq) return BD_ERR_ARG;
+  return bwd_prep_impl(dout, out, gi, workspace, dq, status, stream);
+}
+
+int bd_attn_bwd_main_dq(const void* dout, const void* q, const void* k, const void* v, const float* lse,
+                        const void* seg, const bd_geom* gi, int grad_dtype, float* dq, void* dk, void* dv,
+                        void* workspace, int32_t* status, bd_stream_t stream) {
+  if (!dq) return BD_ERR_ARG;
+  return bwd_main_impl(dout, q, k, v, lse, seg, gi, grad_dtype, dk, dv, workspace, dq, status, stream);
 }
 
 int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* workspace, int32_t* status,
@@ -232,6 +267,12 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return BD_ERR_ARG;
+  if (grad_dtype == BD_DTYPE_F32) {
+    // fp32 dq is its own accumulator: no finalize pass over it
+    float* dqf = static_cast<float*>(dq);
+    if (int rc = bwd_prep_impl(dout, out, gi, workspace, dqf, status, stream)) return rc;
+    return bwd_main_impl(dout, q, k, v, lse, seg, gi, grad_dtype, dk, dv, workspace, dqf, status, stream);
+  }
   if (int rc = bd_attn_bwd_prep(dout, out, gi, workspace, status, stream)) return rc;
   if (int rc = bd_attn_bwd_main(dout, q, k, v, lse, seg, gi, grad_dtype, dk, dv, workspace, status, stream))
     return rc;

@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
-                  const float* __restrict__ delta, float* __restrict__ dq_acc, void* __restrict__ dk,
-                  void* __restrict__ dv, int grads_bf16, int32_t* status) {
+                  const float* __restrict__ delta, float* __restrict__ dq_acc,
+                  void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
   using T = Tiles<D>;
   constexpr int kChunks = T::kChunks;
   constexpr int kChunk = T::kChunk;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < n_real) {
           const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
           l2[e] = lse[row] * 1.4426950408889634f;
-          dl[e] = delta[row];
+          dl[e] = delta[row] * g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
         }
       }
       if (it >= 2 && !warp_wait(&s.q_empty[st], ((it >> 1) - 1) & 1, &s.abort_flag, vstatus)) break;
@@ -410,10 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 4; ++c4) {
           const float4 dl = d4[c4];
           const int c = 16 * h4 + 4 * c4;
-          dsk[2 * c4] = pack_bf16x2(p[c] * (__uint_as_float(sr[4 * c4]) - dl.x),
-                                    p[c + 1] * (__uint_as_float(sr[4 * c4 + 1]) - dl.y));
-          dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(sr[4 * c4 + 2]) - dl.z),
-                                        p[c + 3] * (__uint_as_float(sr[4 * c4 + 3]) - dl.w));
+          dsk[2 * c4] = pack_bf16x2(p[c] * fmaf(__uint_as_float(sr[4 * c4]), g.scale, -dl.x),
+                                    p[c + 1] * fmaf(__uint_as_float(sr[4 * c4 + 1]), g.scale, -dl.y));
+          dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(__uint_as_float(sr[4 * c4 + 2]), g.scale, -dl.z),
+                                        p[c + 3] * fmaf(__uint_as_float(sr[4 * c4 + 3]), g.scale, -dl.w));
         }
         // 32 B of this key row of dS^T (128B-swizzled K-major layout)
 #pragma unroll
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           if (j < g.S_kv) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * g.scale;
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
             store_row(dk, (kv_row0 + j) * D + c, f);
           }
         }

@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (i < n_real) {
           const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
           l2[e] = lse[row] * 1.4426950408889634f;
-          dl[e] = delta[row];
+          dl[e] = delta[row] * g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
         }
       }
       if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
@@ -500,9 +500,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 dl = d4[c4];
         const int c = 4 * c4;
-        pk[2 * c4] = pack_bf16x2(p[c] * (__uint_as_float(sr[c]) - dl.x), p[c + 1] * (__uint_as_float(sr[c + 1]) - dl.y));
+        pk[2 * c4] = pack_bf16x2(p[c] * fmaf(__uint_as_float(sr[c]), g.scale, -dl.x), p[c + 1] * fmaf(__uint_as_float(sr[c + 1]), g.scale, -dl.y));
         pk[2 * c4 + 1] =
-            pack_bf16x2(p[c + 2] * (__uint_as_float(sr[c + 2]) - dl.z), p[c + 3] * (__uint_as_float(sr[c + 3]) - dl.w));
+            pack_bf16x2(p[c + 2] * fmaf(__uint_as_float(sr[c + 2]), g.scale, -dl.z), p[c + 3] * fmaf(__uint_as_float(sr[c + 3]), g.scale, -dl.w));
       }
       if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       // this half's 64 B of the key row of dS^T, 128B-swizzled K-major layout
@@ -535,7 +535,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_wait_ld();
           if (j < g.S_kv) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * g.scale;
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
             store_row(dk, (kv_row0 + j) * D + pass * kDp + c, f);
           }
         }
@@ -659,8 +659,8 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
   const int reach = kv_tiles_reachable(g);
   const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kBwdThreads, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv,
-                                                       bf16, status);
+  kern<<<static_cast<unsigned>(grid), kBwdThreads, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc,
+                                                               dk, dv, bf16, status);
   return cudaGetLastError();
 }
 }  // namespace
@@ -676,13 +676,14 @@ static float* ws_delta(const Geom& g, void* workspace) {
   return reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + align256(rows * g.D * 4));
 }
 
-// K4a: delta and a zeroed dq accumulator.
-cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
-                            cudaStream_t st) {
+// K4a: delta (in the workspace) and a zeroed dq accumulator: `dq_f32` when
+// given (the fp32 dq output itself), else the workspace's.
+cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
+                            int32_t* status, cudaStream_t st) {
   const long long rows = static_cast<long long>(g.B) * g.Hq * g.L;
   const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
   const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(out);
-  float* dq_acc = static_cast<float*>(workspace);
+  float* dq_acc = dq_f32 ? dq_f32 : static_cast<float*>(workspace);
   float* delta = ws_delta(g, workspace);
   const unsigned grid = grid_for(rows * (g.D / 8));
   switch (g.D) {
@@ -702,12 +703,14 @@ cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, co
 // Rows of the q / dout TMA boxes the backward main kernel for this head dim expects.
 int bwd_q_box_rows(int D) { return D <= 128 ? 128 : kBwdQ; }
 
-// K4: dK, dV and the dq accumulation. `mdq` maps the fp32 accumulator at the
-// start of `workspace` as [B*Hq][L][D] with 64 x 64 boxes.
+// K4: dK, dV and the dq accumulation (scale * dS K: the kernels form dS
+// pre-scaled) into the workspace's fp32 accumulator (`mdq` maps it as
+// [B*Hq][L][D] with 64 x 64 boxes) or, when `dq_f32` is given, straight into
+// that fp32 dq output.
 cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                             const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse, void* dk,
-                            void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
-  float* dq_acc = static_cast<float*>(workspace);
+                            void* dv, int bf16, void* workspace, float* dq_f32, int32_t* status, cudaStream_t st) {
+  float* dq_acc = dq_f32 ? dq_f32 : static_cast<float*>(workspace);
   const float* delta = ws_delta(g, workspace);
   {
     const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
@@ -720,16 +723,17 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
     case 64:
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
       return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
-    case 256: return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 256:
+      return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// K4b: dq = scale * accumulator.
+// K4b: dq = the accumulator (already scaled) in the gradient dtype.
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st) {
   const long long n = static_cast<long long>(g.B) * g.Hq * g.L * g.D;
-  dq_convert_kernel<<<grid_for(n / 8), 256, 0, st>>>(static_cast<const float*>(workspace), dq, n, g.scale, bf16,
+  dq_convert_kernel<<<grid_for(n / 8), 256, 0, st>>>(static_cast<const float*>(workspace), dq, n, 1.0f, bf16,
                                                      status);
   return cudaGetLastError();
 }

@@ -272,22 +272,26 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
       tmem_wait_ld();
       const int c0 = (kt_lo + j) * kTile;
-      float x[128];
-      float tmax = -INFINITY;
+      float x[128];  // raw scores, -inf where masked
       if (jlo <= c0 && c0 + kTile - 1 <= jhi) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          x[c] = __uint_as_float(xr[c]) * sl2;
-          tmax = fmaxf(tmax, x[c]);
-        }
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
       } else {
         const int a = jlo - c0, e = jhi - c0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          x[c] = (c >= a && c <= e) ? __uint_as_float(xr[c]) * sl2 : -INFINITY;
-          tmax = fmaxf(tmax, x[c]);
-        }
+        for (int c = 0; c < 128; ++c) x[c] = (c >= a && c <= e) ? __uint_as_float(xr[c]) : -INFINITY;
       }
+      // row max as eight independent 16-column maxima (short dependency chains)
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float a = fmax3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+#pragma unroll
+        for (int c = 16 * k + 3; c < 16 * k + 15; c += 2) a = fmax3(a, x[c], x[c + 1]);
+        mx[k] = fmaxf(a, x[16 * k + 15]);
+      }
+      float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      tmax *= sl2;  // the scale is positive: the max of the scaled scores
       const float m_new = fmaxf(m, tmax);
       const bool need = m_new > m + 8.0f;
       if (__any_sync(0xffffffffu, need)) {
@@ -314,15 +318,17 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
           tmem_wait_st();
         }
       }
-      const float mm = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
+      const float nmm = (m == -INFINITY) ? 0.f : -m;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // row sum in eight partial sums
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(x[2 * c] - mm), p1 = fast_exp2(x[2 * c + 1] - mm);
-        rs += p0 + p1;
+        // exponent: scale * log2(e) * score - max in one FMA
+        const float p0 = fast_exp2(fmaf(x[2 * c], sl2, nmm)), p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, nmm));
+        rs8[c & 7] += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l += rs;
       tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
       tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));

@@ -310,6 +310,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ int elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 // ------------------------------------------------- register redistribution

@@ -104,3 +104,36 @@ def test_cp_union_equals_unsharded():
     torch.testing.assert_close(torch.cat(outs, 2), ref["out"].float(), atol=2e-2, rtol=0)
     torch.testing.assert_close(dks, ref["dk"], atol=2e-2, rtol=0)
     torch.testing.assert_close(dvs, ref["dv"], atol=2e-2, rtol=0)
+
+
+@pytest.mark.parametrize("name", ["d128_g2_ragged", "d256_g2_window"])
+def test_direct_fp32_dq_matches_workspace_accumulator(name):
+    """bd_attn_bwd_prep_dq / _main_dq (fp32 dq as its own accumulator) give the
+    same gradients as prep / main / finalize through the workspace."""
+    from sliding_window_attention_device_gb300 import bdattn
+    w, ranks = next((c[1], c[2]) for c in CASES if c[0] == name)
+    c = make_case(w, ranks[-1])
+    res = run_gpu(c, bwd=False)
+    g, seg, status = res["g"], res["seg"], res["status"]
+    dev = torch.device("cuda")
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    ws = torch.empty(bdattn.bwd_workspace_bytes(g), dtype=torch.uint8, device=dev)
+    out = {}
+    for mode in ("workspace", "direct"):
+        dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.float32, device=dev)
+        dk = torch.full((w.B, w.Hkv, c["S_kv"], w.D), float("nan"), dtype=torch.float32, device=dev)
+        dv = torch.full_like(dk, float("nan"))
+        if mode == "workspace":
+            bdattn.bd_attn_bwd_prep(do, res["out"], g, status, ws)
+            bdattn.bd_attn_bwd_main(do, q, k, v, res["lse"], seg, g, status, ws, dk, dv)
+            bdattn.bd_attn_bwd_finalize(g, status, ws, dq)
+        else:
+            bdattn.bd_attn_bwd_prep_dq(do, res["out"], g, status, ws, dq)
+            bdattn.bd_attn_bwd_main_dq(do, q, k, v, res["lse"], seg, g, status, ws, dq, dk, dv)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        out[mode] = (dq.cpu(), dk.cpu(), dv.cpu())
+    (dq0, dk0, dv0), (dq1, dk1, dv1) = out["workspace"], out["direct"]
+    assert torch.isfinite(dq1).all()
+    torch.testing.assert_close(dq1, dq0, rtol=1e-4, atol=1e-5)
+    assert torch.equal(dk1, dk0) and torch.equal(dv1, dv0)
