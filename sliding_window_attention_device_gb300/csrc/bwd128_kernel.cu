@@ -489,9 +489,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&s.dq_empty);
         }
         if (active) {
+          // these warps issue one red per value and nothing else: a full
+          // tile takes the loop without a per-value row check
+          if (cmax >= kQ) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * hh + c < cmax) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
+            for (int c = 0; c < 64; ++c) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (64 * hh + c < cmax) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
+          }
         }
       }
     }

@@ -602,9 +602,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (active) {
           float* base = dq_acc + ((static_cast<size_t>(b) * g.Hq + h) * g.L) * D + pass * kDp + r;
           const int cmax = min(kBwdQ, n_real - q0);
+          if (cmax >= kBwdQ) {  // full tile: no per-value row check on the red stream
 #pragma unroll
-          for (int c = 0; c < kBwdQ; ++c)
-            if (c < cmax) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+            for (int c = 0; c < kBwdQ; ++c) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBwdQ; ++c)
+              if (c < cmax) red_add_f32(base + static_cast<size_t>(q0 + c) * D, __uint_as_float(qv[c]));
+          }
         }
       }
     }
