@@ -272,8 +272,12 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
       tmem_wait_ld();
       const int c0 = (kt_lo + j) * kTile;
+      // a row either sees the whole tile, none of it (another document, or a
+      // padding row), or part of it (the diagonal / document-start tiles); only
+      // a warp with a partly seen row needs the per-element mask
+      const bool dead = jhi < c0 || jlo > c0 + kTile - 1;
       float x[128];  // raw scores, -inf where masked
-      if (jlo <= c0 && c0 + kTile - 1 <= jhi) {
+      if (__all_sync(0xffffffffu, dead || (jlo <= c0 && c0 + kTile - 1 <= jhi))) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
       } else {
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         mx[k] = fmaxf(a, x[16 * k + 15]);
       }
       float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      tmax *= sl2;  // the scale is positive: the max of the scaled scores
+      tmax = dead ? -INFINITY : tmax * sl2;  // the scale is positive: the max of the scaled scores
       const float m_new = fmaxf(m, tmax);
       const bool need = m_new > m + 8.0f;
       if (__any_sync(0xffffffffu, need)) {
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
           tmem_wait_st();
         }
       }
-      const float nmm = (m == -INFINITY) ? 0.f : -m;
+      // exponent offset; -inf on a row that sees nothing of this tile, so P = 0
+      const float nmm = dead ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
       float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // row sum in eight partial sums
       uint32_t pk[64];
 #pragma unroll
