@@ -265,34 +265,44 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         break;
       }
       tc_fence_after();
+      // S in two halves: the second half's load is in flight while the first
+      // half's max is formed
       uint32_t xr[128];
       tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
       tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
+      tmem_wait_ld();
+      tmem_regs_ready<64>(&xr[0]);
       tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&xr[64]));
       tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
-      tmem_wait_ld();
       const int c0 = (kt_lo + j) * kTile;
       // a row either sees the whole tile, none of it (another document, or a
       // padding row), or part of it (the diagonal / document-start tiles); only
       // a warp with a partly seen row needs the per-element mask
       const bool dead = jhi < c0 || jlo > c0 + kTile - 1;
+      const bool unmasked = __all_sync(0xffffffffu, dead || (jlo <= c0 && c0 + kTile - 1 <= jhi));
+      const int a_lo = jlo - c0, e_hi = jhi - c0;
       float x[128];  // raw scores, -inf where masked
-      if (__all_sync(0xffffffffu, dead || (jlo <= c0 && c0 + kTile - 1 <= jhi))) {
+      float mx[8];   // eight independent 16-column maxima (short dependency chains)
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
-      } else {
-        const int a = jlo - c0, e = jhi - c0;
+      for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1) {
+          tmem_wait_ld();
+          tmem_regs_ready<64>(&xr[64]);
+        }
+        if (unmasked) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = (c >= a && c <= e) ? __uint_as_float(xr[c]) : -INFINITY;
-      }
-      // row max as eight independent 16-column maxima (short dependency chains)
-      float mx[8];
+          for (int c = 64 * hf; c < 64 * hf + 64; ++c) x[c] = __uint_as_float(xr[c]);
+        } else {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float a = fmax3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+          for (int c = 64 * hf; c < 64 * hf + 64; ++c) x[c] = (c >= a_lo && c <= e_hi) ? __uint_as_float(xr[c]) : -INFINITY;
+        }
 #pragma unroll
-        for (int c = 16 * k + 3; c < 16 * k + 15; c += 2) a = fmax3(a, x[c], x[c + 1]);
-        mx[k] = fmaxf(a, x[16 * k + 15]);
+        for (int k = 4 * hf; k < 4 * hf + 4; ++k) {
+          float a = fmax3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+#pragma unroll
+          for (int c = 16 * k + 3; c < 16 * k + 15; c += 2) a = fmax3(a, x[c], x[c + 1]);
+          mx[k] = fmaxf(a, x[16 * k + 15]);
+        }
       }
       float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       tmax = dead ? -INFINITY : tmax * sl2;  // the scale is positive: the max of the scaled scores

@@ -310,6 +310,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// tcgen05.ld writes its destination registers asynchronously; call this right
+// after tcgen05.wait::ld on the registers of the completed loads. The empty
+// volatile statements stay after the wait and every use of the registers
+// depends on them, so no use can be scheduled before the data has arrived.
+template <int N>
+__device__ __forceinline__ void tmem_regs_ready(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
