@@ -13,10 +13,13 @@ What it computes follows the NeMo AutoModel API pages:
   * ``blockdiag_cp.kernels._varlen_seg_for_rank`` /
     ``precompute_blockdiag_varlen_meta`` -- the per-rank varlen segmentation;
   * ``gemma4_moe.cp_local_ring`` (module text) -- bottom-right causal plus a
-    left window for the sliding layer, read as ``p - s < window``.
+    left window for the sliding layer, read as ``p - s < window``; the
+    per-chunk forward over a part of the keys and the ``-inf``-safe online
+    softmax merge of chunk results (``fwd_chunk``, ``merge``).
 
-Every function here is a plain loop in ``bdattn_oracle.c`` (fp64, OpenMP over
-independent rows); this module only marshals arrays.
+Every attention function here is a plain loop in ``bdattn_oracle.c`` (fp64,
+OpenMP over independent rows); ``merge`` is its formula written out in numpy.
+The rest of this module only marshals arrays.
 """
 from __future__ import annotations
 
@@ -71,6 +74,8 @@ def _load():
             lib.og_segments.restype = ctypes.c_int
             lib.og_fwd_rows.argtypes = [P, P, P, P, G, P, ctypes.c_int, P, P]
             lib.og_fwd_rows.restype = ctypes.c_int
+            lib.og_fwd_rows_chunk.argtypes = [P, P, P, P, G, P, ctypes.c_int, P, P]
+            lib.og_fwd_rows_chunk.restype = ctypes.c_int
             lib.og_bwd.argtypes = [P, P, P, P, P, G, P, ctypes.c_int, P, ctypes.c_int, P, P, P]
             lib.og_bwd.restype = ctypes.c_int
             _lib = lib
@@ -174,6 +179,46 @@ def fwd(q, k, v, doc_ids, g: Geom, rows=None):
                                _ptr(out), _ptr(lse)), "fwd")
     if full:
         return out.reshape(g.B, g.Hq, g.L, g.D), lse.reshape(g.B, g.Hq, g.L)
+    return out, lse
+
+
+def fwd_chunk(q, k, v, doc_ids, g: Geom, rows=None):
+    """Forward over one K/V chunk: the K/V buffer [kv_offset, kv_offset + S_kv)
+    holds only part of the keys the rows may attend. Each row gets the softmax
+    over its allowed keys inside the chunk; a real row with none gets out = 0,
+    lse = -inf. Same shapes as fwd()."""
+    qd, kd, vd = _f64(q), _f64(k), _f64(v)
+    doc = _i32(doc_ids).reshape(g.B, g.S_full)
+    assert qd.shape == (g.B, g.Hq, g.L, g.D) and kd.shape == (g.B, g.Hkv, g.S_kv, g.D) == vd.shape
+    full = rows is None
+    sel = _all_rows(g) if full else np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = sel.shape[0]
+    out = np.zeros((n, g.D), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    _check(_load().og_fwd_rows_chunk(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(doc), ctypes.byref(g), _ptr(sel), n,
+                                     _ptr(out), _ptr(lse)), "fwd_chunk")
+    if full:
+        return out.reshape(g.B, g.Hq, g.L, g.D), lse.reshape(g.B, g.Hq, g.L)
+    return out, lse
+
+
+def merge(out_a, lse_a, out_b, lse_b):
+    """Log-sum-exp merge of two chunk results (gemma4_moe.cp_local_ring: online
+    softmax merge of per-chunk (out, lse), safe when either or both are -inf):
+        lse = log(exp(lse_a) + exp(lse_b))
+        out = exp(lse_a - lse) out_a + exp(lse_b - lse) out_b
+    A row with both lse = -inf gets out = 0, lse = -inf. fp64."""
+    oa, ob = np.asarray(out_a, np.float64), np.asarray(out_b, np.float64)
+    la, lb = np.asarray(lse_a, np.float64), np.asarray(lse_b, np.float64)
+    m = np.maximum(la, lb)
+    both_empty = np.isneginf(m)
+    ms = np.where(both_empty, 0.0, m)
+    ea, eb = np.exp(la - ms), np.exp(lb - ms)  # exp(-inf) = 0 for an empty side
+    tot = ea + eb
+    lse = np.where(both_empty, -np.inf, ms + np.log(np.where(both_empty, 1.0, tot)))
+    wa = np.where(both_empty, 0.0, ea / np.where(both_empty, 1.0, tot))
+    wb = np.where(both_empty, 0.0, eb / np.where(both_empty, 1.0, tot))
+    out = wa[..., None] * oa + wb[..., None] * ob
     return out, lse
 
 

@@ -287,6 +287,48 @@ int og_fwd_rows(const double* q, const double* k, const double* v, const int32_t
   return err;
 }
 
+/* Forward of one K/V chunk (the keys of the K/V buffer only) for rows
+ * sel[n][3]: the softmax over the allowed keys that lie in the chunk. A real
+ * row with no allowed key in the chunk gets out = 0 and lse = -inf, the
+ * identity of the log-sum-exp merge of chunk results (gemma4_moe.cp_local_ring
+ * per-chunk forward and `-inf`-safe merge). */
+int og_fwd_rows_chunk(const double* q, const double* k, const double* v, const int32_t* doc, const og_geom* g,
+                      const int32_t* sel, int n, double* out, double* lse) {
+  if (!og_geom_ok(g) || !q || !k || !v || !doc || !sel || !out || !lse) return OG_ERR_ARG;
+  int err = OG_OK;
+#pragma omp parallel
+  {
+    double* xbuf = (double*)malloc(sizeof(double) * (size_t)(g->S_kv > 0 ? g->S_kv : 1));
+    if (!xbuf) {
+#pragma omp atomic write
+      err = OG_ERR_NOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int t = 0; t < n; ++t) {
+        const int b = sel[3 * t], h = sel[3 * t + 1], i = sel[3 * t + 2];
+        if (b < 0 || b >= g->B || h < 0 || h >= g->Hq || i < 0 || i >= g->L) {
+#pragma omp atomic write
+          err = OG_ERR_ARG;
+          continue;
+        }
+        double* o = out + (size_t)t * g->D;
+        int r = og_fwd_row(q, k, v, doc, g, b, h, i, o, lse + t, xbuf);
+        if (r == OG_ERR_EMPTY_ROW) {
+          for (int d = 0; d < g->D; ++d) o[d] = 0.0;
+          lse[t] = -INFINITY;
+          r = OG_OK;
+        }
+        if (r != OG_OK) {
+#pragma omp atomic write
+          err = r;
+        }
+      }
+      free(xbuf);
+    }
+  }
+  return err;
+}
+
 /* ------------------------------------------------------------ backward --- */
 
 /* Analytic backward of the loss sum(out * dout) for selected query rows
