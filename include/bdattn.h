@@ -138,6 +138,30 @@ int bd_attn_seg_layout(const bd_geom* g, int32_t* offsets /* >= BD_SEG_NOFF + 3 
  * n_seg = 0 and s_first = real_end = row_offset. */
 int bd_attn_seg_build(const int32_t* doc_ids, const bd_geom* g, void* seg, int32_t* status, bd_stream_t stream);
 
+/* The same table for one chunk of the K/V range (gemma4_moe.cp_local_ring:
+ * the per-step forward over the K/V chunk a ring step holds). The K/V buffer
+ * [kv_offset, kv_offset + S_kv) need not contain every key the local rows may
+ * attend, so KV_RANGE is never set; bd_attn_fwd then gives each row the
+ * softmax over its allowed keys inside the chunk, with out = 0 and lse = -inf
+ * for a row that has none, and bd_attn_bwd_main (with the merged out / lse
+ * of all chunks, through bd_attn_bwd_prep) adds the chunk's share of dq and
+ * writes the chunk's dk / dv. Merge chunk forwards with bd_attn_merge. */
+int bd_attn_seg_build_chunk(const int32_t* doc_ids, const bd_geom* g, void* seg, int32_t* status,
+                            bd_stream_t stream);
+
+/* Log-sum-exp merge of a chunk's forward result into a running one, in place
+ * (gemma4_moe.cp_local_ring: -inf-safe online softmax merge):
+ *   lse = log(exp(lse) + exp(lse_chunk)),
+ *   out = exp(lse_old - lse) out + exp(lse_chunk - lse) out_chunk,
+ * in fp32 per element. A side with lse = -inf has weight 0 whatever its out
+ * holds, so a running result may start as lse = -inf with any out; a row
+ * empty on both sides stays out = 0, lse = -inf.
+ * out, out_chunk: bf16 [B,Hq,L,D], 16-byte aligned; lse, lse_chunk: fp32
+ * [B,Hq,L]. Device pointers, caller-owned; BD_ERR_ARG for null or misaligned
+ * pointers. Does nothing if *status is already nonzero. */
+int bd_attn_merge(void* out, float* lse, const void* out_chunk, const float* lse_chunk, const bd_geom* g,
+                  int32_t* status, bd_stream_t stream);
+
 /* Step 2: forward. out = softmax(scale * q k^T + mask) v per query row,
  * lse = natural-log sum of exp(scale * q.k) over the allowed keys.
  * Padding rows: out = 0, lse = -inf. Needs the table from
@@ -170,7 +194,11 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
  *  _main:     dk, dv (written in full) and the dq accumulation (of the final,
  *             scaled gradient) in `workspace`;
  *  _finalize: dq = accumulator, converted to grad_dtype.
- * They must run in this order on one stream with the same workspace. */
+ * They must run in this order on one stream with the same workspace. With the
+ * K/V range split into chunks (bd_attn_seg_build_chunk), run _prep once with
+ * the merged out, then _main once per chunk (that chunk's geometry, table,
+ * k, v, dk, dv and the merged lse; B, Hq, Hkv, D, S_full, L, row_offset and
+ * window as in _prep), then _finalize: dq is the sum over the chunks. */
 int bd_attn_bwd_prep(const void* dout, const void* out, const bd_geom* g, void* workspace, int32_t* status,
                      bd_stream_t stream);
 int bd_attn_bwd_main(const void* dout, const void* q, const void* k, const void* v, const float* lse,

@@ -31,7 +31,8 @@ HDR_WORDS = 32
 REGIONS = ("hdr", "cu_q", "cu_k", "row_lo", "qt_krange", "kt_qrange", "full_bits", "fwd_work", "bwd_work",
            "counts", "total")
 
-EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_fwd",
+EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_seg_build_chunk",
+           "bd_attn_fwd", "bd_attn_merge",
            "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
            "bd_attn_bwd_finalize", "bd_attn_bwd_prep_dq", "bd_attn_bwd_main_dq",
            "bd_attn_bwd_noalloc", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
@@ -78,6 +79,10 @@ def load() -> ctypes.CDLL:
         lib.bd_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.bd_attn_seg_build.argtypes = [P, G, P, P, P]
         lib.bd_attn_seg_build.restype = ctypes.c_int
+        lib.bd_attn_seg_build_chunk.argtypes = [P, G, P, P, P]
+        lib.bd_attn_seg_build_chunk.restype = ctypes.c_int
+        lib.bd_attn_merge.argtypes = [P, P, P, P, G, P, P]
+        lib.bd_attn_merge.restype = ctypes.c_int
         lib.bd_attn_fwd.argtypes = [P, P, P, P, G, P, P, P, P]
         lib.bd_attn_fwd.restype = ctypes.c_int
         lib.bd_attn_bwd.argtypes = [P, P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
@@ -171,6 +176,34 @@ def bd_attn_seg_build(doc_ids: torch.Tensor, g: Geom, seg: torch.Tensor | None =
     _check(load().bd_attn_seg_build(_ptr(doc_ids), ctypes.byref(g), _ptr(seg), _ptr(status), _stream(stream)),
            "bd_attn_seg_build")
     return seg, status
+
+
+def bd_attn_seg_build_chunk(doc_ids: torch.Tensor, g: Geom, seg: torch.Tensor | None = None,
+                            status: torch.Tensor | None = None, stream=None):
+    """Segment table for one chunk of the K/V range (no K/V range requirement); returns (seg, status)."""
+    dev = doc_ids.device
+    _need(doc_ids, "doc_ids", torch.int32, (g.B, g.S_full), None)
+    if seg is None:
+        seg = torch.empty(seg_bytes(g) // 4, dtype=torch.int32, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    _check(load().bd_attn_seg_build_chunk(_ptr(doc_ids), ctypes.byref(g), _ptr(seg), _ptr(status),
+                                          _stream(stream)), "bd_attn_seg_build_chunk")
+    return seg, status
+
+
+def bd_attn_merge(out, lse, out_chunk, lse_chunk, g: Geom, status, stream=None):
+    """Merge a K/V chunk's (out, lse) into the running (out, lse), in place."""
+    dev = out.device
+    for name, t in (("out", out), ("out_chunk", out_chunk)):
+        _need(t, name, torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    for name, t in (("lse", lse), ("lse_chunk", lse_chunk)):
+        _need(t, name, torch.float32, (g.B, g.Hq, g.L), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    _check(load().bd_attn_merge(_ptr(out), _ptr(lse), _ptr(out_chunk), _ptr(lse_chunk), ctypes.byref(g),
+                                _ptr(status), _stream(stream)), "bd_attn_merge")
 
 
 def bd_attn_fwd(q, k, v, seg, g: Geom, status, out=None, lse=None, stream=None):

@@ -12,7 +12,10 @@
 #include "sm100_ptx.cuh"
 
 namespace bd {
-cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st);
+cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st,
+                             int kv_chunk);
+cudaError_t launch_merge(const Geom& g, void* out, float* lse, const void* out_c, const float* lse_c,
+                         const int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
 cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
@@ -157,7 +160,28 @@ int bd_attn_seg_build(const int32_t* doc_ids, const bd_geom* gi, void* seg, int3
   if (int rc = to_geom(gi, &g)) return rc;
   if (!doc_ids || !seg || !status || !aligned16(seg)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
-  return cuda_rc(launch_seg_build(doc_ids, g, static_cast<int32_t*>(seg), status, static_cast<cudaStream_t>(stream)));
+  return cuda_rc(
+      launch_seg_build(doc_ids, g, static_cast<int32_t*>(seg), status, static_cast<cudaStream_t>(stream), 0));
+}
+
+int bd_attn_seg_build_chunk(const int32_t* doc_ids, const bd_geom* gi, void* seg, int32_t* status,
+                            bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!doc_ids || !seg || !status || !aligned16(seg)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(
+      launch_seg_build(doc_ids, g, static_cast<int32_t*>(seg), status, static_cast<cudaStream_t>(stream), 1));
+}
+
+int bd_attn_merge(void* out, float* lse, const void* out_chunk, const float* lse_chunk, const bd_geom* gi,
+                  int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (!out || !lse || !out_chunk || !lse_chunk || !status) return BD_ERR_ARG;
+  if (!aligned16(out) || !aligned16(out_chunk)) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_merge(g, out, lse, out_chunk, lse_chunk, status, static_cast<cudaStream_t>(stream)));
 }
 
 int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,

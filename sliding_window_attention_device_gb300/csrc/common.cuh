@@ -44,7 +44,8 @@ __host__ __device__ inline void seg_layout(int B, int L, int S_kv, int* off, int
 
 // Header words that record the geometry the table was built for.
 constexpr int kHdrRowOffset = 16, kHdrL = 17, kHdrKvOffset = 18, kHdrSkv = 19, kHdrWindow = 20,
-              kHdrSfull = 21, kHdrMagic = 22;
+              kHdrSfull = 21, kHdrMagic = 22,
+              kHdrKvChunk = 23;  // 1: table built for one K/V chunk (no K/V range requirement)
 constexpr int kSegMagic = 0x62646174;  // "bdat"
 
 // The allowed key interval [lo, hi] (global positions) of a real local row i:

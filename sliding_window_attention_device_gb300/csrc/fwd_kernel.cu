@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       const int p = g.row_offset + i;
       const int doc_start = seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i];
       jlo = row_lo_window(doc_start, p, g.window) - g.kv_offset;
-      jhi = p - g.kv_offset;
+      jhi = min(p - g.kv_offset, g.S_kv - 1);  // a K/V chunk may end before the row
     }
     const float sl2 = g.scale * 1.4426950408889634f;
     float m = -INFINITY, l = 0.f;

@@ -72,7 +72,7 @@ __device__ int block_exclusive_scan(int v, int* s_red, int* total) {
 
 // One CTA per batch row.
 __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restrict__ doc, Geom g,
-                                                         int32_t* __restrict__ seg, int32_t* status) {
+                                                         int32_t* __restrict__ seg, int32_t* status, int kv_chunk) {
   __shared__ int s_red[32];
   const int b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
   const int ro = g.row_offset, L = g.L;
@@ -194,7 +194,8 @@ __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restri
   if (tid == 0) {
     cu_k[n_seg] = real_end - s_first;
     const int need_lo = n_real > 0 ? row_lo_window(s_first, ro, g.window) : ro;
-    const int kv_bad = n_real > 0 && (need_lo < g.kv_offset || real_end > g.kv_offset + g.S_kv);
+    // a chunk of the K/V range need not hold every key the rows may attend
+    const int kv_bad = !kv_chunk && n_real > 0 && (need_lo < g.kv_offset || real_end > g.kv_offset + g.S_kv);
     const int row_status = (bad ? BD_STATUS_LAYOUT : 0) | (kv_bad ? BD_STATUS_KV_RANGE : 0);
     hdr[BD_SEG_N_REAL] = n_real;
     hdr[BD_SEG_N_SEG] = n_seg;
@@ -214,8 +215,9 @@ __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restri
     hdr[kHdrSkv] = g.S_kv;
     hdr[kHdrWindow] = g.window;
     hdr[kHdrSfull] = g.S_full;
+    hdr[kHdrKvChunk] = kv_chunk;
     hdr[kHdrMagic] = kSegMagic;
-    for (int x = kHdrMagic + 1; x < BD_SEG_HDR_WORDS; ++x) hdr[x] = 0;
+    for (int x = kHdrKvChunk + 1; x < BD_SEG_HDR_WORDS; ++x) hdr[x] = 0;
     if (row_status) atomicOr(status, row_status);
   }
 }
@@ -346,8 +348,9 @@ __global__ void __launch_bounds__(1024) classify_kernel(Geom g, int32_t* __restr
   }
 }
 
-cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st) {
-  seg_build_kernel<<<g.B, 1024, 0, st>>>(doc, g, seg, status);
+cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st,
+                             int kv_chunk) {
+  seg_build_kernel<<<g.B, 1024, 0, st>>>(doc, g, seg, status, kv_chunk);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // histogram bins of the work-list sort (48 KB of shared memory at most)
