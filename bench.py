@@ -12,6 +12,12 @@ segmentation + tile classification, forward, backward (prep, main, dq
 finalize). Inputs are resident in HBM before the timed region; K/V (268 MB)
 exceed the 129 MB L2, so no flush is needed between steps.
 
+With --kv-chunks ring, each shard's K/V arrives in per-rank pieces as in a
+ring step: a forward per piece merged into the shard's (out, lse) by the
+log-sum-exp merge kernel, then one backward main per piece with the merged
+out / lse. The FLOP count is the same; the line adds the merge kernel's HBM
+roofline.
+
 With --gpus N (torchrun), each GPU runs an independent replica with its own
 seed (weak scaling; no collective on the data path).
 """
@@ -243,13 +249,106 @@ class Replica:
             self.run_shard(i, ev)
 
 
+class RingChunkReplica(Replica):
+    """The same shards with K/V arriving in pieces, as one ring step at a time
+    (gemma4_moe.cp_local_ring, the ring forward loop: per step the K/V block of
+    one context-parallel rank, a varlen forward over it returning (out, lse),
+    the -inf-safe merge, and a per-chunk backward with the merged out / lse).
+    A shard's K/V range is cut at the ranks' boundaries [j L, (j+1) L); blocks
+    owned by a rank after the shard's own are skipped, as the loop skips them
+    (no local row reaches a later position), and so are blocks wholly before
+    every local row's sliding window. Each chunk has its own table,
+    contiguous K / V and dK / dV; the first chunk's forward writes the shard's
+    out / lse, the others go through a scratch (out, lse) and the merge kernel."""
+
+    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None):
+        super().__init__(w, seed, dev, grad_dtype, ranks)
+        bd = self.bd
+        kv_cache = {}
+        self.launches_per_step = 0
+        for s, sh in zip(self.shards, self.plan):
+            lo, hi = sh["kv_offset"], sh["kv_offset"] + sh["S_kv"]
+            chunks = []
+            for j in range(sh["r"] + 1):
+                a, b = max(lo, j * w.L), min(hi, (j + 1) * w.L)
+                if b <= a or (w.window > 0 and b <= sh["row_offset"] - w.window + 1):
+                    continue  # empty, or wholly before every local row's window
+                if (a, b) not in kv_cache:
+                    kv_cache[(a, b)] = (self.k_full[:, :, a:b].contiguous(), self.v_full[:, :, a:b].contiguous())
+                g = bd.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, sh["row_offset"], a, b - a, w.window)
+                k, v = kv_cache[(a, b)]
+                chunks.append(dict(g=g, k=k, v=v, seg=torch.empty(bd.seg_bytes(g) // 4, dtype=torch.int32, device=dev),
+                                   dk=torch.empty(w.B, w.Hkv, b - a, w.D, dtype=grad_dtype, device=dev),
+                                   dv=torch.empty(w.B, w.Hkv, b - a, w.D, dtype=grad_dtype, device=dev)))
+            if not chunks:
+                raise ValueError(f"shard r={sh['r']}: no K/V chunk")
+            s["chunks"] = chunks
+            n = len(chunks)
+            # per chunk: table build + classification, forward, zero-fill + backward
+            # main; per merge one launch; per shard the backward prep (and the dq
+            # finalize for bf16 gradients)
+            self.launches_per_step += 5 * n + (n - 1) + 1 + (0 if grad_dtype == torch.float32 else 1)
+        self.n_merges = sum(len(s["chunks"]) - 1 for s in self.shards)
+        self.kv_chunk_bytes = sum(k.numel() * 2 + v.numel() * 2 for k, v in kv_cache.values())
+        self.out_c = torch.empty(w.B, w.Hq, w.L, w.D, dtype=torch.bfloat16, device=dev)
+        self.lse_c = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
+
+    def merge_bytes(self) -> float:
+        """Algorithmic bytes of one merge launch: read both (out, lse), write one."""
+        w = self.w
+        rows = w.B * w.Hq * w.L
+        return 3.0 * rows * (w.D * 2 + 4)
+
+    def run_shard(self, i, ev=None):
+        bd = self.bd
+        s = self.shards[i]
+        ws = self.workspace[:bd.bwd_workspace_bytes(s["g"])]
+        for c in s["chunks"]:
+            bd.bd_attn_seg_build_chunk(self.doc, c["g"], seg=c["seg"], status=self.status)
+        if ev is not None:
+            ev["fwd"][i][0].record()
+        for n, c in enumerate(s["chunks"]):
+            if n == 0:
+                bd.bd_attn_fwd(s["q"], c["k"], c["v"], c["seg"], c["g"], self.status, out=s["out"], lse=s["lse"])
+                continue
+            bd.bd_attn_fwd(s["q"], c["k"], c["v"], c["seg"], c["g"], self.status, out=self.out_c, lse=self.lse_c)
+            if ev is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            bd.bd_attn_merge(s["out"], s["lse"], self.out_c, self.lse_c, c["g"], self.status)
+            if ev is not None:
+                e1.record()
+                ev["merge"].append((e0, e1))
+        if ev is not None:
+            ev["fwd"][i][1].record()
+        direct = s["dq"].dtype == torch.float32
+        if direct:
+            bd.bd_attn_bwd_prep_dq(s["do"], s["out"], s["g"], self.status, ws, s["dq"])
+        else:
+            bd.bd_attn_bwd_prep(s["do"], s["out"], s["g"], self.status, ws)
+        if ev is not None:
+            ev["bwd"][i][0].record()
+        for c in s["chunks"]:
+            if direct:
+                bd.bd_attn_bwd_main_dq(s["do"], s["q"], c["k"], c["v"], s["lse"], c["seg"], c["g"], self.status,
+                                       ws, s["dq"], c["dk"], c["dv"])
+            else:
+                bd.bd_attn_bwd_main(s["do"], s["q"], c["k"], c["v"], s["lse"], c["seg"], c["g"], self.status, ws,
+                                    c["dk"], c["dv"])
+        if ev is not None:
+            ev["bwd"][i][1].record()
+        if not direct:
+            bd.bd_attn_bwd_finalize(s["g"], self.status, ws, s["dq"])
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.config]
     grad_dtype = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
     ranks = None if args.shards is None else {int(x) for x in args.shards.split(",")}
-    rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks)
+    chunked = args.kv_chunks == "ring"
+    rep = (RingChunkReplica if chunked else Replica)(w, args.seed + rank, dev, grad_dtype, ranks)
     total_flop, fwd_flop, bwd_flop = rep.flops()
 
     def barrier():
@@ -264,7 +363,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     n = len(rep.shards)
     ev_steps = [{"fwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
-                 "bwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]}
+                 "bwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
+                 "merge": []}
                 for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
@@ -284,6 +384,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ms = start.elapsed_time(stop)
     fwd_ms = sum(e["fwd"][i][0].elapsed_time(e["fwd"][i][1]) for e in ev_steps for i in range(n))
     bwd_ms = sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
+    merge_ms = sum(a.elapsed_time(b) for e in ev_steps for a, b in e["merge"])
+    n_merge = sum(len(e["merge"]) for e in ev_steps)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -291,7 +393,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ms_per_step = ms / args.steps
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not chunked:
         e2e = run_e2e(rep, args, total_flop, world)
 
     if rank != 0:
@@ -301,8 +403,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     traffic = None
-    if TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha():
-        traffic = TRAFFIC["bytes_per_launch"]
+    if TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked:
+        traffic = TRAFFIC["bytes_per_launch"]  # measured per whole-shard launch, not per chunk
+    n_bwd = sum(len(s["chunks"]) for s in rep.shards) if chunked else len(rep.shards)
+    fwd_kernel_ms = fwd_ms - merge_ms  # the forward region less its merges
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -310,21 +414,34 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "config": {"workload": f"{w.key}: {w.title}", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "S": w.S,
                    "cp_size": w.cp_size, "L": w.L, "ranks": [s["r"] for s in rep.plan], "window": w.window, "kv": w.kv,
                    "grad_dtype": args.grad_dtype, "l2": "inputs larger than L2 (K/V 268 MB), no flush",
-                   "pairs": sum(s["pairs"] for s in rep.shards), "seed": args.seed},
+                   "pairs": sum(s["pairs"] for s in rep.shards), "seed": args.seed,
+                   "kv_chunks": ("ring: K/V cut at the cp ranks' boundaries, owners after the shard skipped, "
+                                 f"{n_bwd} chunks, {rep.n_merges} merges per step") if chunked else "none"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
-        "fwd_tflops": round(fwd_flop * args.steps / (fwd_ms * 1e-3) / 1e12, 2),
+        "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
         "roofline": {"kernel": "bwd128_kernel<128> (backward main stage, with its dK/dV zero-fill launch)", "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
                      "traffic": traffic,
-                     "flops_per_launch": bwd_flop / len(rep.shards),
-                     "avg_launch_ms": round(bwd_ms / (args.steps * len(rep.shards)), 4)},
+                     "flops_per_launch": bwd_flop / n_bwd,
+                     "avg_launch_ms": round(bwd_ms / (args.steps * n_bwd), 4)},
         "gpu_launches": rep.launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": e2e,
     }
+    if chunked:
+        line["e2e_note"] = "end-to-end timing is taken on the unchunked path only"
+        if n_merge:
+            merge_s = merge_ms * 1e-3 / n_merge
+            achieved = rep.merge_bytes() / merge_s / 1e9
+            line["merge_roofline"] = {
+                "kernel": f"merge_kernel<{w.D}>", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_launch": rep.merge_bytes(),
+                "avg_launch_ms": round(merge_ms / n_merge, 4), "launches": n_merge,
+                "share_of_step": round(merge_ms / ms, 4)}
     return line
 
 
@@ -493,6 +610,8 @@ def main():
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32")
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kv-chunks", choices=("none", "ring"), default="none",
+                    help="ring: each shard's K/V in per-rank chunks, forward merged, backward per chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=32,
                     help="query heads of batch row 0 in the oracle's timed CPU-baseline slice")

@@ -159,3 +159,48 @@ def test_merge_edge_cases():
     np.testing.assert_allclose(got_out, ref_out, rtol=0, atol=2e-2)
     assert (got_out[..., 64:96, :] == 0).all()
     np.testing.assert_array_equal(got_out[..., 32:64, :], a.double().numpy()[..., 32:64, :])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("key,r", [("C2", 3), ("C2", 7), ("C3", 7), ("C5w512", 5)])
+def test_ring_chunks_full_size_sampled(key, r):
+    """Full size, through the chunking and calls the benchmark's ring mode times:
+    sampled rows (out, lse, dq) and keys (dk, dv) against the oracle over the
+    whole K/V range; keys in a skipped block get no gradient from any row; and
+    sum over all keys of dV equals the sum of dO over the real rows."""
+    import bench
+    from test_gpu_full import _oracle_sampled, _pick, _check
+    w = synth.WORKLOADS[key]
+    dev = torch.device("cuda")
+    rep = bench.RingChunkReplica(w, 0, dev, torch.float32, ranks={r})
+    rep.step()
+    torch.cuda.synchronize()
+    assert int(rep.status.item()) == 0
+    s = rep.shards[0]
+    c = make_case(w, r, seed=0)
+    assert (c["kv_offset"], c["S_kv"]) == (s["g"].kv_offset, s["g"].S_kv)
+    rows, keys = _pick(c, np.random.default_rng(321))
+    ref_rows, ref_keys = _oracle_sampled(c, rows, keys)
+    out, lse, dq = s["out"].float().cpu(), s["lse"].cpu(), s["dq"].cpu()
+    for (b, h, i), (o_ref, l_ref, dq_ref) in ref_rows.items():
+        _check(f"{key} r{r} out[{b},{h},{i}]", out[b, h, i].numpy(), o_ref)
+        _check(f"{key} r{r} dq[{b},{h},{i}]", dq[b, h, i].numpy(), dq_ref)
+        if np.isneginf(l_ref):
+            assert torch.isneginf(lse[b, h, i])
+        else:
+            assert abs(float(lse[b, h, i]) - l_ref) <= LSE_ABS
+    for (b, hk, j), (dk_ref, dv_ref) in ref_keys.items():
+        pos = c["kv_offset"] + j
+        ch = [x for x in s["chunks"] if x["g"].kv_offset <= pos < x["g"].kv_offset + x["g"].S_kv]
+        if not ch:  # a skipped block: no local row may reach it
+            assert not np.any(dk_ref) and not np.any(dv_ref), (key, r, b, hk, j)
+            continue
+        jj = pos - ch[0]["g"].kv_offset
+        _check(f"{key} r{r} dk[{b},{hk},{j}]", ch[0]["dk"][b, hk, jj].cpu().numpy(), dk_ref)
+        _check(f"{key} r{r} dv[{b},{hk},{j}]", ch[0]["dv"][b, hk, jj].cpu().numpy(), dv_ref)
+    real = torch.from_numpy(c["doc"][:, c["row_offset"]:c["row_offset"] + w.L] != 0).to(dev)
+    do = s["do"].double() * real[:, None, :, None]
+    lhs = sum(x["dv"].double().sum(2) for x in s["chunks"])
+    rhs = do.view(w.B, w.Hkv, w.G, w.L, w.D).sum((2, 3))
+    rel = ((lhs - rhs).norm() / rhs.norm().clamp_min(1e-30)).item()
+    assert rel < 1e-2, f"{key} r{r}: sum dV identity rel err {rel:.3e}"
