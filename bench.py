@@ -18,6 +18,11 @@ log-sum-exp merge kernel, then one backward main per piece with the merged
 out / lse. The FLOP count is the same; the line adds the merge kernel's HBM
 roofline.
 
+With --exchange, the line is instead the sender side of the needed-only
+K/V exchange for every rank of the workload: the exchange plan built from the
+device doc ids, the gather of K and V into the send buffers and the index-add
+of the returned dK / dV, in algorithmic GB/s against the HBM roofline.
+
 With --gpus N (torchrun), each GPU runs an independent replica with its own
 seed (weak scaling; no collective on the data path).
 """
@@ -341,6 +346,123 @@ class RingChunkReplica(Replica):
             bd.bd_attn_bwd_finalize(s["g"], self.status, ws, s["dq"])
 
 
+def run_exchange(args, local_rank: int) -> dict:
+    """The sender side of the needed-only K/V exchange for every virtual rank of
+    the workload (blockdiag_cp.exchange: the exchange plan from the device doc
+    ids, `_NeededKVExchange` forward gather of K and V into the token-major send
+    buffer, and its backward index-add of the returned dK / dV): one step runs
+    all four for every rank. Inputs resident in HBM; the collective between
+    GPUs is not part of it."""
+    from sliding_window_attention_device_gb300 import bdattn as bd
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.config]
+    W, L = w.cp_size, w.L
+    doc_np = synth.doc_layout(w.layout, w.B, w.S, args.seed)
+    doc = torch.from_numpy(doc_np).to(dev)
+    k, v = synth.kv_rows(w, args.seed)
+    k, v = k.to(dev), v.to(dev)
+    status = bd.new_status(dev)
+    # the send-buffer sizes come from the plans, read back once before timing
+    plans = [bd.bd_attn_exchange_plan(doc, W, r, status=status)[0] for r in range(W)]
+    p = bd.read_plan(plans[0], w.B, W, L)
+    ranks = []
+    for r in range(W):
+        n = sum(p["counts"][r])
+        gen = torch.Generator(device=dev).manual_seed(args.seed * 100 + r)
+        ranks.append(dict(
+            plan=plans[r], n=n,
+            k=k[:, :, r * L:(r + 1) * L].contiguous(), v=v[:, :, r * L:(r + 1) * L].contiguous(),
+            sk=torch.empty((max(n, 1), w.B, w.Hkv, w.D), dtype=torch.bfloat16, device=dev),
+            sv=torch.empty((max(n, 1), w.B, w.Hkv, w.D), dtype=torch.bfloat16, device=dev),
+            gk=torch.rand((max(n, 1), w.B, w.Hkv, w.D), generator=gen, device=dev),
+            gv=torch.rand((max(n, 1), w.B, w.Hkv, w.D), generator=gen, device=dev),
+            dk=torch.empty((w.B, w.Hkv, L, w.D), dtype=torch.float32, device=dev),
+            dv=torch.empty((w.B, w.Hkv, L, w.D), dtype=torch.float32, device=dev)))
+    del k, v
+    kinds = ("plan", "gather", "scatter_add")
+
+    def phase(kind):
+        for i, s in enumerate(ranks):
+            if kind == "plan":
+                bd.bd_attn_exchange_plan(doc, W, i, plan=s["plan"], status=status)
+            elif kind == "gather":
+                bd.bd_attn_needed_gather(s["k"], s["plan"], s["sk"], status)
+                bd.bd_attn_needed_gather(s["v"], s["plan"], s["sv"], status)
+            else:
+                bd.bd_attn_needed_scatter_add(s["gk"], s["plan"], s["dk"], status)
+                bd.bd_attn_needed_scatter_add(s["gv"], s["plan"], s["dv"], status)
+
+    # Each phase (every rank's plans, gathers or index-adds) is one CUDA graph:
+    # the launches are small enough that issuing them one by one from Python
+    # would leave the GPU waiting on the host.
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(args.warmup):
+            for kd in kinds:
+                phase(kd)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} after warm-up")
+    graphs = {}
+    for kd in kinds:
+        graphs[kd] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graphs[kd]):
+            phase(kd)
+    for _ in range(args.warmup):
+        for kd in kinds:
+            graphs[kd].replay()
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(str(local_rank)) as clk:
+        torch.cuda.synchronize()
+        start.record()
+        for m in events:
+            m[0].record()
+            for j, kd in enumerate(kinds):
+                graphs[kd].replay()
+                m[j + 1].record()
+        stop.record()
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item()):#x} in the timed region")
+    ms = start.elapsed_time(stop)
+    kind_ms = {kd: sum(m[j].elapsed_time(m[j + 1]) for m in events) for j, kd in enumerate(kinds)}
+    row = w.B * w.Hkv * w.D  # elements per token
+    sent = sum(s["n"] for s in ranks)
+    # algorithmic bytes per step: the gathers read each local chunk once and write
+    # the send buffers (K and V, bf16); the index-adds read the returned fp32
+    # gradients and write the local dK / dV once
+    gather_bytes = 2 * (W * L * row * 2 + sent * row * 2)
+    scatter_bytes = 2 * (sent * row * 4 + W * L * row * 4)
+    peaks = read_peaks()
+    steps = args.steps
+
+    def roof(kind, nbytes):
+        t = kind_ms[kind] * 1e-3 / steps
+        return {"kernel": kind, "bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(nbytes / t / 1e9 / peaks["hbm_gbs"], 4), "bytes_per_step": nbytes,
+                "ms_per_step": round(kind_ms[kind] / steps, 4), "launches_per_step": 2 * W}
+
+    value = (gather_bytes + scatter_bytes) / (ms * 1e-3 / steps) / 1e9
+    return {
+        "metric": "needed-only K/V exchange, sender side (plan + gather + index-add), algorithmic GB/s, 1 GPU",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / steps, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 K/V, f32 gradients", "data": "synthetic",
+        "config": {"workload": f"{w.key}: {w.title}", "B": w.B, "Hkv": w.Hkv, "D": w.D, "S": w.S, "cp_size": W,
+                   "L": L, "use_halo": bool(p["use_halo"]), "halo_size": p["halo_size"], "tokens_sent": sent,
+                   "seed": args.seed, "l2": "send buffers and gradients of all ranks exceed L2 together; no flush"},
+        "plan_us_per_rank": round(kind_ms["plan"] * 1e3 / (steps * W), 2),
+        "roofline": roof("gather", gather_bytes), "roofline_index_add": roof("scatter_add", scatter_bytes),
+        "gpu_launches": 6 * W * steps, "launch": "one CUDA graph per phase (plans, gathers, index-adds of every rank)",
+        "clocks": clk.summary(),
+    }
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -610,6 +732,8 @@ def main():
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32")
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--exchange", action="store_true",
+                    help="time the sender side of the needed-only K/V exchange (plan, gather, index-add) instead")
     ap.add_argument("--kv-chunks", choices=("none", "ring"), default="none",
                     help="ring: each shard's K/V in per-rank chunks, forward merged, backward per chunk")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -635,6 +759,10 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     from sliding_window_attention_device_gb300 import build as _build
     _build.build()
+    if args.exchange:
+        if rank == 0:
+            print(json.dumps(run_exchange(args, local_rank)), flush=True)
+        return
     try:
         line = run_ours(args, rank, world, local_rank)
         if line is not None:

@@ -248,6 +248,99 @@ int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const vo
                         const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk,
                         void* dv, int32_t* status, bd_stream_t stream);
 
+/* ---- K/V exchange plans (blockdiag_cp.exchange) --------------------------
+ *
+ * The global left-halo plan and the needed-only all-to-all-v split plan,
+ * computed on the device from the replicated doc ids with no host
+ * synchronisation, and the sender's local halves of the needed-only exchange
+ * (`_NeededKVExchange`): the gather of the send buffer and the index-add of
+ * the returned gradients. The collective that moves the buffers between GPUs
+ * is not part of this library.
+ *
+ * The sequence of S_full positions splits into cp_size equal chunks of
+ * L = S_full / cp_size; rank r owns [r*L, (r+1)*L). Rank r needs the K/V
+ * range [s_first_r, real_end_r): real_end_r = r*L + its real local rows,
+ * s_first_r = the first position of the run of equal ids holding r*L (the
+ * straddle of its first document). With B > 1 the range covers every batch
+ * row's range (rows whose local rows are all padding do not count); a rank
+ * with no real row at all needs nothing: s_first = real_end = r*L.
+ *   back_r = r*L - s_first_r;  use_halo = (back_r <= L for every rank);
+ *   halo_size = max_r back_r   (the uniform-size neighbour exchange; rank r
+ *                               keeps the last back_r tokens it receives);
+ *   counts[src][dst] = |[src*L, (src+1)*L) intersect [s_first_dst, real_end_dst)|;
+ *   for this plan's rank:  in_splits[dst] = counts[rank][dst] (send counts),
+ *   out_splits[src] = counts[src][rank] (receive counts), send_off / recv_off
+ *   their exclusive prefix sums, and send_index = the local positions
+ *   (0..L-1) of the send buffer's tokens, destination by destination, each
+ *   destination's piece in increasing position. The receiver's pieces, in
+ *   source order, make its needed range.
+ *
+ * The plan is an int32 array (device, caller-owned, 16-byte aligned) of
+ * bd_attn_plan_bytes(B, cp_size, L) bytes, regions at the word offsets that
+ * bd_attn_plan_layout returns (BD_PLAN_OFF_* order). */
+#define BD_PLAN_HDR_WORDS 16
+#define BD_PLAN_MAGIC 0        /* header word: 0x62647870 once built */
+#define BD_PLAN_CP_SIZE 1
+#define BD_PLAN_L 2
+#define BD_PLAN_RANK 3
+#define BD_PLAN_B 4
+#define BD_PLAN_USE_HALO 5
+#define BD_PLAN_HALO_SIZE 6
+#define BD_PLAN_TOTAL_SEND 7   /* sum of in_splits = send buffer tokens */
+#define BD_PLAN_TOTAL_RECV 8   /* sum of out_splits = real_end_rank - s_first_rank */
+
+#define BD_PLAN_OFF_HDR 0         /* [16]          header */
+#define BD_PLAN_OFF_S_FIRST 1     /* [cp_size]     s_first of every rank */
+#define BD_PLAN_OFF_REAL_END 2    /* [cp_size]     real_end of every rank */
+#define BD_PLAN_OFF_BACK 3        /* [cp_size]     back_r (= halo tokens rank r receives from r - 1) */
+#define BD_PLAN_OFF_HALO_SEND 4   /* [cp_size]     halo tokens rank r sends to r + 1 (= back_{r+1}; 0 for the last) */
+#define BD_PLAN_OFF_COUNTS 5      /* [cp_size][cp_size]  counts[src][dst] */
+#define BD_PLAN_OFF_IN_SPLITS 6   /* [cp_size]     this rank's per-destination send counts */
+#define BD_PLAN_OFF_OUT_SPLITS 7  /* [cp_size]     this rank's per-source receive counts */
+#define BD_PLAN_OFF_SEND_OFF 8    /* [cp_size]     exclusive prefix sums of in_splits */
+#define BD_PLAN_OFF_RECV_OFF 9    /* [cp_size]     exclusive prefix sums of out_splits */
+#define BD_PLAN_OFF_SEND_INDEX 10 /* [cp_size * L] send_index (first TOTAL_SEND entries) */
+#define BD_PLAN_OFF_ROW_RANGE 11  /* [B][cp_size][2]  scratch of the build */
+#define BD_PLAN_OFF_TOTAL 12      /* total words */
+#define BD_PLAN_NOFF 13
+
+/* Bytes of a plan (0 for an invalid size: B, cp_size or L < 1, cp_size >
+ * 1024, or cp_size * L beyond 2^31 - 1). */
+size_t bd_attn_plan_bytes(int B, int cp_size, int L);
+/* Word offsets of the plan's regions into offsets[BD_PLAN_NOFF]. */
+int bd_attn_plan_layout(int B, int cp_size, int L, int32_t* offsets);
+
+/* Build the plan of rank `rank` from doc_ids int32 [B, S_full] (device).
+ * S_full must be a multiple of cp_size. Two kernels: per (rank, batch row)
+ * the real rows and the run start, then the plan. Sets BD_STATUS_LAYOUT (and
+ * still writes the plan) for a negative id or a real id after padding
+ * inside a chunk. BD_ERR_ARG for a null or misaligned pointer, an invalid
+ * size or rank. */
+int bd_attn_exchange_plan(const int32_t* doc_ids, int B, int S_full, int cp_size, int rank, void* plan,
+                          int32_t* status, bd_stream_t stream);
+
+/* Forward of the needed-only exchange on the sender: the send buffer
+ * send[j][b][c][:] = x_local[b][c][send_index[j]][:] for j < TOTAL_SEND, in
+ * the token-major layout [max_rows][B][C][D] so that each destination's piece
+ * is one contiguous block (starting at token send_off[dst]). x_local is
+ * [B][C][L][D]; dtype BD_DTYPE_BF16 or BD_DTYPE_F32; D * element size a
+ * multiple of 16 bytes. The token count is read from the plan on the device:
+ * when it exceeds max_rows, BD_STATUS_BOUNDS is set and nothing is written
+ * (max_rows = cp_size * L always suffices). Does nothing if *status is
+ * already nonzero. B and L must match the plan's (else BD_STATUS_BOUNDS). */
+int bd_attn_needed_gather(const void* x_local, const void* plan, int B, int C, int L, int D, int dtype, void* send,
+                          int max_rows, int32_t* status, bd_stream_t stream);
+
+/* Backward of the needed-only exchange on the sender (the index-add): the
+ * gradients of the send buffer, grad_send [max_rows][B][C][D] (first
+ * TOTAL_SEND tokens used), summed onto their source tokens:
+ * grad_local[b][c][t][:] = sum over destinations whose piece holds t, in
+ * destination order, of that token's gradient, accumulated in fp32; 0 for a
+ * token no destination needs. grad_local [B][C][L][D] is written in full.
+ * Deterministic. Same dtype, size and status rules as bd_attn_needed_gather. */
+int bd_attn_needed_scatter_add(const void* grad_send, const void* plan, int B, int C, int L, int D, int dtype,
+                               void* grad_local, int max_rows, int32_t* status, bd_stream_t stream);
+
 /* Human-readable text for a host return code. */
 const char* bd_attn_strerror(int code);
 

@@ -35,7 +35,16 @@ EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_a
            "bd_attn_fwd", "bd_attn_merge",
            "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
            "bd_attn_bwd_finalize", "bd_attn_bwd_prep_dq", "bd_attn_bwd_main_dq",
-           "bd_attn_bwd_noalloc", "bd_attn_strerror", "bd_attn_selftest_wait_timeout")
+           "bd_attn_bwd_noalloc", "bd_attn_plan_bytes", "bd_attn_plan_layout", "bd_attn_exchange_plan",
+           "bd_attn_needed_gather", "bd_attn_needed_scatter_add", "bd_attn_strerror",
+           "bd_attn_selftest_wait_timeout")
+
+# exchange plan: header fields (BD_PLAN_*) and regions (BD_PLAN_OFF_*)
+PLAN_HDR_FIELDS = ("magic", "cp_size", "L", "rank", "B", "use_halo", "halo_size", "total_send", "total_recv")
+PLAN_HDR_WORDS = 16
+PLAN_REGIONS = ("hdr", "s_first", "real_end", "back", "halo_send", "counts", "in_splits", "out_splits", "send_off",
+                "recv_off", "send_index", "row_range", "total")
+PLAN_MAGIC = 0x62647870
 
 
 class Geom(ctypes.Structure):
@@ -97,6 +106,17 @@ def load() -> ctypes.CDLL:
         lib.bd_attn_bwd_prep_dq.restype = ctypes.c_int
         lib.bd_attn_bwd_main_dq.argtypes = [P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
         lib.bd_attn_bwd_main_dq.restype = ctypes.c_int
+        I = ctypes.c_int
+        lib.bd_attn_plan_bytes.argtypes = [I, I, I]
+        lib.bd_attn_plan_bytes.restype = ctypes.c_size_t
+        lib.bd_attn_plan_layout.argtypes = [I, I, I, P]
+        lib.bd_attn_plan_layout.restype = I
+        lib.bd_attn_exchange_plan.argtypes = [P, I, I, I, I, P, P, P]
+        lib.bd_attn_exchange_plan.restype = I
+        lib.bd_attn_needed_gather.argtypes = [P, P, I, I, I, I, I, P, I, P, P]
+        lib.bd_attn_needed_gather.restype = I
+        lib.bd_attn_needed_scatter_add.argtypes = [P, P, I, I, I, I, I, P, I, P, P]
+        lib.bd_attn_needed_scatter_add.restype = I
         lib.bd_attn_strerror.argtypes = [ctypes.c_int]
         lib.bd_attn_strerror.restype = ctypes.c_char_p
         lib.bd_attn_selftest_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
@@ -368,3 +388,85 @@ def read_seg(seg: torch.Tensor, g: Geom) -> dict:
             "bwd_work": a[lay["bwd_work"]: lay["bwd_work"] + B * nkt].copy(),
             "counts": a[lay["counts"]: lay["counts"] + 4].copy(),
             "layout": lay}
+
+
+# ------------------------------------------------------------ exchange plans
+def plan_bytes(B: int, cp_size: int, L: int) -> int:
+    n = load().bd_attn_plan_bytes(int(B), int(cp_size), int(L))
+    if n == 0:
+        raise ValueError(f"invalid plan size B={B} cp_size={cp_size} L={L}")
+    return int(n)
+
+
+def plan_layout(B: int, cp_size: int, L: int) -> dict:
+    arr = (ctypes.c_int32 * len(PLAN_REGIONS))()
+    _check(load().bd_attn_plan_layout(int(B), int(cp_size), int(L), arr), "bd_attn_plan_layout")
+    return {name: int(arr[i]) for i, name in enumerate(PLAN_REGIONS)}
+
+
+def bd_attn_exchange_plan(doc_ids: torch.Tensor, cp_size: int, rank: int, plan: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None, stream=None):
+    """Exchange plan of `rank` from the replicated doc ids [B, S] (device); returns (plan, status)."""
+    dev = doc_ids.device
+    B, S = doc_ids.shape
+    _need(doc_ids, "doc_ids", torch.int32, (B, S), None)
+    if S % cp_size:
+        raise ValueError("the sequence must split into cp_size equal chunks")
+    n = plan_bytes(B, cp_size, S // cp_size) // 4
+    if plan is None:
+        plan = torch.empty(n, dtype=torch.int32, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _need(plan, "plan", torch.int32, (n,), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    _check(load().bd_attn_exchange_plan(_ptr(doc_ids), int(B), int(S), int(cp_size), int(rank), _ptr(plan),
+                                        _ptr(status), _stream(stream)), "bd_attn_exchange_plan")
+    return plan, status
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BD_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return BD_DTYPE_F32
+    raise ValueError("bfloat16 or float32 expected")
+
+
+def bd_attn_needed_gather(x_local: torch.Tensor, plan: torch.Tensor, send: torch.Tensor, status, stream=None):
+    """send [max_rows, B, C, D] (token-major) from x_local [B, C, L, D] by the plan's send_index."""
+    B, C, L, D = x_local.shape
+    max_rows = send.shape[0]
+    _need(x_local, "x_local", x_local.dtype, (B, C, L, D), None)
+    _need(send, "send", x_local.dtype, (max_rows, B, C, D), x_local.device)
+    _need(status, "status", torch.int32, (1,), x_local.device)
+    _check(load().bd_attn_needed_gather(_ptr(x_local), _ptr(plan), B, C, L, D, _dtype_code(x_local), _ptr(send),
+                                        int(max_rows), _ptr(status), _stream(stream)), "bd_attn_needed_gather")
+    return send
+
+
+def bd_attn_needed_scatter_add(grad_send: torch.Tensor, plan: torch.Tensor, grad_local: torch.Tensor, status,
+                               stream=None):
+    """grad_local [B, C, L, D] = the index-add of grad_send [max_rows, B, C, D] (token-major)."""
+    B, C, L, D = grad_local.shape
+    max_rows = grad_send.shape[0]
+    _need(grad_local, "grad_local", grad_local.dtype, (B, C, L, D), None)
+    _need(grad_send, "grad_send", grad_local.dtype, (max_rows, B, C, D), grad_local.device)
+    _need(status, "status", torch.int32, (1,), grad_local.device)
+    _check(load().bd_attn_needed_scatter_add(_ptr(grad_send), _ptr(plan), B, C, L, D, _dtype_code(grad_local),
+                                             _ptr(grad_local), int(max_rows), _ptr(status), _stream(stream)),
+           "bd_attn_needed_scatter_add")
+    return grad_local
+
+
+def read_plan(plan: torch.Tensor, B: int, cp_size: int, L: int) -> dict:
+    """Copy a plan to the host and decode it (synchronises; tests and tools only)."""
+    lay = plan_layout(B, cp_size, L)
+    a = plan.cpu().numpy()
+    W = cp_size
+    h = a[lay["hdr"]: lay["hdr"] + PLAN_HDR_WORDS]
+    d = {name: int(h[i]) for i, name in enumerate(PLAN_HDR_FIELDS)}
+    for name in ("s_first", "real_end", "back", "halo_send", "in_splits", "out_splits", "send_off", "recv_off"):
+        d[name] = [int(x) for x in a[lay[name]: lay[name] + W]]
+    d["counts"] = [[int(x) for x in a[lay["counts"] + s * W: lay["counts"] + (s + 1) * W]] for s in range(W)]
+    d["send_index"] = [int(x) for x in a[lay["send_index"]: lay["send_index"] + max(0, d["total_send"])]]
+    return d

@@ -26,6 +26,12 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st);
 size_t bwd_workspace_bytes(const Geom& g);
+cudaError_t launch_exchange_plan(const int32_t* doc, int B, int S, int W, int rank, int32_t* plan, int32_t* status,
+                                 cudaStream_t st);
+cudaError_t launch_needed_gather(const void* x, const int32_t* plan, int B, int C, int L, int vshift, void* send,
+                                 int max_rows, int32_t* status, cudaStream_t st);
+cudaError_t launch_needed_scatter_add(const void* gsend, const int32_t* plan, int B, int C, int L, int vshift,
+                                      int bf16, void* glocal, int max_rows, int32_t* status, cudaStream_t st);
 int bwd_q_box_rows(int D);
 
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t limit_ns) {
@@ -129,6 +135,23 @@ int make_map_f32(CUtensorMap* m, const void* ptr, int D, int rows, int planes) {
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
 
+// Rows of D elements of `dtype` as 16-byte vectors: log2 of the vectors per
+// row, or -1 when a row is not a power-of-two number of vectors or an index
+// of a [max_rows][B][C] or [B][C][L] array of them would pass 2^31.
+int exchange_vshift(int B, int C, int L, int D, int dtype, int max_rows) {
+  if (B < 1 || C < 1 || L < 1 || D < 1 || max_rows < 0) return -1;
+  if (dtype != BD_DTYPE_F32 && dtype != BD_DTYPE_BF16) return -1;
+  const long long bytes = static_cast<long long>(D) * (dtype == BD_DTYPE_F32 ? 4 : 2);
+  if (bytes % 16) return -1;
+  const long long vpr = bytes / 16;
+  if (vpr & (vpr - 1)) return -1;
+  int sh = 0;
+  while ((1LL << sh) < vpr) ++sh;
+  const long long bc = static_cast<long long>(B) * C;
+  if (((bc * L) << sh) > 0x7fffffffLL || ((bc * max_rows) << sh) > 0x7fffffffLL) return -1;
+  return sh;
+}
+
 }  // namespace
 
 extern "C" {
@@ -182,6 +205,52 @@ int bd_attn_merge(void* out, float* lse, const void* out_chunk, const float* lse
   if (!aligned16(out) || !aligned16(out_chunk)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
   return cuda_rc(launch_merge(g, out, lse, out_chunk, lse_chunk, status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t bd_attn_plan_bytes(int B, int cp_size, int L) {
+  int off[BD_PLAN_NOFF];
+  const long long words = plan_layout(B, cp_size, L, off);
+  return words < 0 ? 0 : static_cast<size_t>(words) * 4;
+}
+
+int bd_attn_plan_layout(int B, int cp_size, int L, int32_t* offsets) {
+  int off[BD_PLAN_NOFF];
+  if (!offsets || plan_layout(B, cp_size, L, off) < 0) return BD_ERR_ARG;
+  for (int i = 0; i < BD_PLAN_NOFF; ++i) offsets[i] = off[i];
+  return BD_OK;
+}
+
+int bd_attn_exchange_plan(const int32_t* doc_ids, int B, int S_full, int cp_size, int rank, void* plan,
+                          int32_t* status, bd_stream_t stream) {
+  if (!doc_ids || !plan || !status || !aligned16(plan)) return BD_ERR_ARG;
+  if (B < 1 || cp_size < 1 || S_full < 1 || S_full % cp_size || rank < 0 || rank >= cp_size) return BD_ERR_ARG;
+  if (B > 65535 || bd_attn_plan_bytes(B, cp_size, S_full / cp_size) == 0) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_exchange_plan(doc_ids, B, S_full, cp_size, rank, static_cast<int32_t*>(plan), status,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_needed_gather(const void* x_local, const void* plan, int B, int C, int L, int D, int dtype, void* send,
+                          int max_rows, int32_t* status, bd_stream_t stream) {
+  if (!x_local || !plan || !send || !status) return BD_ERR_ARG;
+  if (!aligned16(x_local) || !aligned16(plan) || !aligned16(send)) return BD_ERR_ARG;
+  const int sh = exchange_vshift(B, C, L, D, dtype, max_rows);
+  if (sh < 0) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_needed_gather(x_local, static_cast<const int32_t*>(plan), B, C, L, sh, send, max_rows,
+                                      status, static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_needed_scatter_add(const void* grad_send, const void* plan, int B, int C, int L, int D, int dtype,
+                               void* grad_local, int max_rows, int32_t* status, bd_stream_t stream) {
+  if (!grad_send || !plan || !grad_local || !status) return BD_ERR_ARG;
+  if (!aligned16(grad_send) || !aligned16(plan) || !aligned16(grad_local)) return BD_ERR_ARG;
+  const int sh = exchange_vshift(B, C, L, D, dtype, max_rows);
+  if (sh < 0) return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  return cuda_rc(launch_needed_scatter_add(grad_send, static_cast<const int32_t*>(plan), B, C, L, sh,
+                                           dtype == BD_DTYPE_BF16, grad_local, max_rows, status,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,

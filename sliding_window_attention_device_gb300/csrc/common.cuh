@@ -42,6 +42,25 @@ __host__ __device__ inline void seg_layout(int B, int L, int S_kv, int* off, int
   off[BD_SEG_OFF_TOTAL] = o;
 }
 
+// Exchange plan layout (BD_PLAN_OFF_* regions, each on a 16-byte boundary).
+// Returns the total words, or -1 when a size is out of range.
+constexpr int kPlanMagic = 0x62647870;  // "bdxp"
+constexpr int kPlanMaxRanks = 1024;
+__host__ __device__ inline long long plan_layout(int B, int W, int L, int* off) {
+  if (B < 1 || W < 1 || L < 1 || W > kPlanMaxRanks) return -1;
+  if (static_cast<long long>(W) * L > 0x7fffffffLL || static_cast<long long>(B) * W > (1 << 24)) return -1;
+  long long o = 0;
+  long long sz[BD_PLAN_OFF_TOTAL] = {BD_PLAN_HDR_WORDS, W, W, W, W, static_cast<long long>(W) * W, W, W, W, W,
+                                     static_cast<long long>(W) * L, 2LL * B * W};
+  for (int i = 0; i < BD_PLAN_OFF_TOTAL; ++i) {
+    off[i] = static_cast<int>(o);
+    o = (o + sz[i] + 3) & ~3LL;
+    if (o > 0x7fffffffLL) return -1;
+  }
+  off[BD_PLAN_OFF_TOTAL] = static_cast<int>(o);
+  return o;
+}
+
 // Header words that record the geometry the table was built for.
 constexpr int kHdrRowOffset = 16, kHdrL = 17, kHdrKvOffset = 18, kHdrSkv = 19, kHdrWindow = 20,
               kHdrSfull = 21, kHdrMagic = 22,

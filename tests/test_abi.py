@@ -85,3 +85,24 @@ def test_null_pointers_rejected(lib):
                            P(256), P(16), None) == bdattn.BD_ERR_ARG
     assert lib.bd_attn_selftest_wait_timeout(None, 1000, None) == bdattn.BD_ERR_ARG
     assert bdattn.strerror(bdattn.BD_ERR_ARG).startswith("invalid argument")
+
+
+def test_plan_constants_and_layout(lib):
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define\s+(BD_PLAN_\w+)\s+(0x[0-9a-fA-F]+|\d+)", text))
+    for i, name in enumerate(bdattn.PLAN_HDR_FIELDS):
+        assert int(consts[f"BD_PLAN_{name.upper()}"], 0) == i
+    assert int(consts["BD_PLAN_HDR_WORDS"]) == bdattn.PLAN_HDR_WORDS
+    assert int(consts["BD_PLAN_NOFF"]) == len(bdattn.PLAN_REGIONS)
+    for i, name in enumerate(bdattn.PLAN_REGIONS):
+        assert int(consts[f"BD_PLAN_OFF_{name.upper()}"]) == i
+    B, W, L = 3, 8, 100
+    lay = bdattn.plan_layout(B, W, L)
+    sizes = dict(hdr=16, s_first=W, real_end=W, back=W, halo_send=W, counts=W * W, in_splits=W, out_splits=W,
+                 send_off=W, recv_off=W, send_index=W * L, row_range=2 * B * W)
+    names = bdattn.PLAN_REGIONS
+    for a, b in zip(names[:-1], names[1:]):
+        assert lay[a] % 4 == 0 and lay[b] - lay[a] >= sizes[a] and lay[b] - lay[a] < sizes[a] + 4
+    assert bdattn.plan_bytes(B, W, L) == 4 * lay["total"]
+    assert lib.bd_attn_plan_bytes(0, 8, 100) == 0 and lib.bd_attn_plan_bytes(1, 1025, 4) == 0
+    assert lib.bd_attn_exchange_plan(None, 1, 64, 4, 0, None, None, None) == bdattn.BD_ERR_ARG
