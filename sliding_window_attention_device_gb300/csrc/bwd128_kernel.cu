@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
                   const float* __restrict__ delta, float* __restrict__ dq_acc,
                   void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
+  pdl_begin();
   using T = Tiles<D>;
   constexpr int kChunks = T::kChunks;
   constexpr int kChunk = T::kChunk;
@@ -539,8 +540,8 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   const int reach = kv_tiles_reachable(g);
   const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16,
-                                                            status);
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, mq, mdo,
+      mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace

@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       const __nv_bfloat16* __restrict__ out,
                                                       float* __restrict__ delta, float* __restrict__ dq_acc,
                                                       long long n_rows, const int32_t* status) {
+  pdl_begin();
   if (*reinterpret_cast<const volatile int*>(status) != 0) return;
   constexpr int kLanes = D / 8;  // threads per row, 8 elements (16 B) each
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ dq_acc, void* __restrict__ dq,
                                                          long long n_elems, float scale, int to_bf16,
                                                          const int32_t* status) {
+  pdl_begin();
   if (*reinterpret_cast<const volatile int*>(status) != 0) return;
   const long long n8 = n_elems / 8;
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                const __grid_constant__ CUtensorMap tm_dq, const int32_t* __restrict__ seg, const Geom g,
                const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dq_acc,
                void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
+  pdl_begin();
   using Cfg = BwdCfg<D>;
   constexpr int NSQ = Cfg::kNsq, kDp = Cfg::kDp, kPasses = Cfg::kPasses;
   using Smem = BwdSmem<D, NSQ>;
@@ -636,6 +639,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // the zeros (every (tile, kv head) pair past the attended ones in the work list).
 __global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const int32_t* __restrict__ seg, const Geom g, void* dk,
                                                           void* dv, int grads_bf16, int32_t* status) {
+  pdl_begin();
   const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
   if (n_att < 0 || n_att > g.B * g.nkt) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, BD_STATUS_BOUNDS);
@@ -664,8 +668,8 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
   const int reach = kv_tiles_reachable(g);
   const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), kBwdThreads, smem, st>>>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc,
-                                                               dk, dv, bf16, status);
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kBwdThreads), smem, st, mq,
+      mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace
@@ -692,9 +696,12 @@ cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, vo
   float* delta = ws_delta(g, workspace);
   const unsigned grid = grid_for(rows * (g.D / 8));
   switch (g.D) {
-    case 64: bwd_pre_kernel<64><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
-    case 128: bwd_pre_kernel<128><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
-    case 256: bwd_pre_kernel<256><<<grid, 256, 0, st>>>(dob, ob, delta, dq_acc, rows, status); break;
+    case 64: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<64>, dim3(grid), dim3(256), 0, st, dob, ob, delta,
+        dq_acc, rows, status); le != cudaSuccess) return le; break;
+    case 128: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<128>, dim3(grid), dim3(256), 0, st, dob, ob,
+        delta, dq_acc, rows, status); le != cudaSuccess) return le; break;
+    case 256: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<256>, dim3(grid), dim3(256), 0, st, dob, ob,
+        delta, dq_acc, rows, status); le != cudaSuccess) return le; break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -720,7 +727,8 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
   {
     const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
     const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
-    bwd_zero_kv_kernel<<<grid, 256, 0, st>>>(seg, g, dk, dv, bf16, status);
+    if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
+        status); le != cudaSuccess) return le;
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -738,8 +746,8 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st) {
   const long long n = static_cast<long long>(g.B) * g.Hq * g.L * g.D;
-  dq_convert_kernel<<<grid_for(n / 8), 256, 0, st>>>(static_cast<const float*>(workspace), dq, n, 1.0f, bf16,
-                                                     status);
+  if (const cudaError_t le = launch_pdl(dq_convert_kernel, dim3(grid_for(n / 8)), dim3(256), 0, st,
+      static_cast<const float*>(workspace), dq, n, 1.0f, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

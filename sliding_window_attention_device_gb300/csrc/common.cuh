@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include "bdattn.h"  // include/ is on the include path
 
 namespace bd {
@@ -86,6 +87,35 @@ __host__ __device__ inline int kv_tiles_reachable(const Geom& g) {
 }
 
 #ifdef __CUDACC__
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization and starts with pdl_begin(): it waits
+// (griddepcontrol.wait) until the grids before it in the stream have completed
+// and their memory is visible -- so it touches no global memory before that --
+// and then lets the next grid launch (griddepcontrol.launch_dependents). A
+// dependent grid launches only once every CTA of this one has started, so its
+// CTAs take only resources this grid leaves free; what it gains is that its
+// CTAs are already resident when this grid ends, instead of launching then.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class... Exp, class... Act>
+inline cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Act&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
+
 // Zero dK / dV rows of the K/V tiles no local row attends. The backward work
 // list holds the n_att attended tiles first; the (position, kv head) pairs of
 // the rest, x = (z - n_att) * Hkv + hk, are taken by writer w of n_w as

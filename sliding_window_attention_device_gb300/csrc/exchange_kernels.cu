@@ -46,6 +46,7 @@ __device__ int cta_allreduce(int v, Op op, int* s_red) {
 
 __global__ void __launch_bounds__(kPlanThreads) plan_rows_kernel(const int32_t* __restrict__ doc, int B, int S, int W,
                                                                 int L, int32_t* __restrict__ plan, int32_t* status) {
+  pdl_begin();
   const int r = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, nthr = blockDim.x;
   int off[BD_PLAN_NOFF];
   plan_layout(B, W, L, off);
@@ -108,6 +109,7 @@ __device__ __forceinline__ int piece(int src, int L, int lo_dst, int hi_dst) {
 __global__ void __launch_bounds__(kPlanThreads) plan_finish_kernel(const int32_t* __restrict__ doc, int B, int S,
                                                                   int W, int L, int rank,
                                                                   int32_t* __restrict__ plan) {
+  pdl_begin();
   __shared__ int s_red[32];
   __shared__ int s_lo[kPlanMaxRanks], s_hi[kPlanMaxRanks], s_soff[kPlanMaxRanks];
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(kCopyThreads) needed_gather_kernel(const uint4
                                                                     const int32_t* __restrict__ plan, int B, int BC,
                                                                     int L, int vshift, uint4* __restrict__ send,
                                                                     int max_rows, int32_t* status) {
+  pdl_begin();
   if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
   if (!plan_usable(plan, B, L, max_rows, status)) return;
   const int W = plan[BD_PLAN_CP_SIZE], n = plan[BD_PLAN_TOTAL_SEND];
@@ -264,6 +267,7 @@ __global__ void __launch_bounds__(kCopyThreads) needed_scatter_add_kernel(const 
                                                                          int BC, int L, int vshift,
                                                                          uint4* __restrict__ glocal, int max_rows,
                                                                          int32_t* status) {
+  pdl_begin();
   __shared__ int s_a[kPlanMaxRanks], s_e[kPlanMaxRanks], s_o[kPlanMaxRanks];
   if (*reinterpret_cast<const volatile int32_t*>(status) != 0) return;
   if (!plan_usable(plan, B, L, max_rows, status)) return;
@@ -352,19 +356,21 @@ unsigned copy_grid(long long elems) {
 cudaError_t launch_exchange_plan(const int32_t* doc, int B, int S, int W, int rank, int32_t* plan, int32_t* status,
                                  cudaStream_t st) {
   const int L = S / W;
-  plan_rows_kernel<<<dim3(W, B), kPlanThreads, 0, st>>>(doc, B, S, W, L, plan, status);
+  if (const cudaError_t le = launch_pdl(plan_rows_kernel, dim3(dim3(W, B)), dim3(kPlanThreads), 0, st, doc, B, S, W,
+      L, plan, status); le != cudaSuccess) return le;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  plan_finish_kernel<<<1, kPlanThreads, 0, st>>>(doc, B, S, W, L, rank, plan);
+  if (const cudaError_t le = launch_pdl(plan_finish_kernel, dim3(1), dim3(kPlanThreads), 0, st, doc, B, S, W, L,
+      rank, plan); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
 cudaError_t launch_needed_gather(const void* x, const int32_t* plan, int B, int C, int L, int vshift, void* send,
                                  int max_rows, int32_t* status, cudaStream_t st) {
   const long long elems = (static_cast<long long>(max_rows) * B * C) << vshift;
-  needed_gather_kernel<<<copy_grid<needed_gather_kernel>(elems), kCopyThreads, 0, st>>>(static_cast<const uint4*>(x), plan, B, B * C, L,
-                                                                  vshift, static_cast<uint4*>(send), max_rows,
-                                                                  status);
+  if (const cudaError_t le = launch_pdl(needed_gather_kernel, dim3(copy_grid<needed_gather_kernel>(elems)),
+      dim3(kCopyThreads), 0, st, static_cast<const uint4*>(x), plan, B, B * C, L, vshift, static_cast<uint4*>(send),
+      max_rows, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
@@ -373,13 +379,12 @@ cudaError_t launch_needed_scatter_add(const void* gsend, const int32_t* plan, in
   const long long elems = (static_cast<long long>(B) * C * L) << vshift;
   const auto* g = static_cast<const uint4*>(gsend);
   auto* o = static_cast<uint4*>(glocal);
-  if (bf16)
-    needed_scatter_add_kernel<true><<<copy_grid<needed_scatter_add_kernel<true>>(elems), kCopyThreads, 0, st>>>(g, plan, B, B * C, L, vshift, o,
-                                                                               max_rows, status);
-  else
-    needed_scatter_add_kernel<false><<<copy_grid<needed_scatter_add_kernel<false>>(elems), kCopyThreads, 0, st>>>(g, plan, B, B * C, L, vshift, o,
-                                                                                max_rows, status);
-  return cudaGetLastError();
+  const cudaError_t e =
+      bf16 ? launch_pdl(needed_scatter_add_kernel<true>, dim3(copy_grid<needed_scatter_add_kernel<true>>(elems)),
+                        dim3(kCopyThreads), 0, st, g, plan, B, B * C, L, vshift, o, max_rows, status)
+           : launch_pdl(needed_scatter_add_kernel<false>, dim3(copy_grid<needed_scatter_add_kernel<false>>(elems)),
+                        dim3(kCopyThreads), 0, st, g, plan, B, B * C, L, vshift, o, max_rows, status);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace bd

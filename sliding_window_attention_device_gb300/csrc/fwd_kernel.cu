@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
                __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t* status) {
+  pdl_begin();
   using Smem = FwdSmem<D, NQ, NS>;
   using TM = FwdTmem<D, NQ>;
   constexpr int kChunks = Smem::kChunks;
@@ -401,7 +402,8 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), 128 + NQ * 128, smem, st>>>(mq, mk, mv, seg, g, out, lse, status);
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(128 + NQ * 128), smem, st, mq,
+      mk, mv, seg, g, out, lse, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) merge_kernel(__nv_bfloat16* __restrict__ 
                                                     const __nv_bfloat16* __restrict__ out_c,
                                                     const float* __restrict__ lse_c, long long rows,
                                                     const int32_t* status) {
+  pdl_begin();
   constexpr int kPerRow = D / 8;           // 16-byte pieces per row
   constexpr int kRowsPerWarp = 32 / kPerRow;
   static_assert(32 % kPerRow == 0, "a warp holds whole rows");
@@ -82,9 +83,12 @@ cudaError_t launch_merge(const Geom& g, void* out, float* lse, const void* out_c
   auto* o = static_cast<__nv_bfloat16*>(out);
   auto* oc = static_cast<const __nv_bfloat16*>(out_c);
   switch (g.D) {
-    case 64: merge_kernel<64><<<grid, 256, 0, st>>>(o, lse, oc, lse_c, rows, status); break;
-    case 128: merge_kernel<128><<<grid, 256, 0, st>>>(o, lse, oc, lse_c, rows, status); break;
-    case 256: merge_kernel<256><<<grid, 256, 0, st>>>(o, lse, oc, lse_c, rows, status); break;
+    case 64: if (const cudaError_t le = launch_pdl(merge_kernel<64>, dim3(grid), dim3(256), 0, st, o, lse, oc, lse_c,
+        rows, status); le != cudaSuccess) return le; break;
+    case 128: if (const cudaError_t le = launch_pdl(merge_kernel<128>, dim3(grid), dim3(256), 0, st, o, lse, oc,
+        lse_c, rows, status); le != cudaSuccess) return le; break;
+    case 256: if (const cudaError_t le = launch_pdl(merge_kernel<256>, dim3(grid), dim3(256), 0, st, o, lse, oc,
+        lse_c, rows, status); le != cudaSuccess) return le; break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -73,6 +73,7 @@ __device__ int block_exclusive_scan(int v, int* s_red, int* total) {
 // One CTA per batch row.
 __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restrict__ doc, Geom g,
                                                          int32_t* __restrict__ seg, int32_t* status, int kv_chunk) {
+  pdl_begin();
   __shared__ int s_red[32];
   const int b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
   const int ro = g.row_offset, L = g.L;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restri
 // A single CTA classifies every tile of every batch row and builds the two
 // longest-first work lists. Dynamic shared memory: (nbins) ints of histogram.
 __global__ void __launch_bounds__(1024) classify_kernel(Geom g, int32_t* __restrict__ seg, int nbins) {
+  pdl_begin();
   extern __shared__ int s_hist[];
   __shared__ int s_red[32];
   const int tid = threadIdx.x, nthr = blockDim.x;
@@ -350,13 +352,15 @@ __global__ void __launch_bounds__(1024) classify_kernel(Geom g, int32_t* __restr
 
 cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, int32_t* status, cudaStream_t st,
                              int kv_chunk) {
-  seg_build_kernel<<<g.B, 1024, 0, st>>>(doc, g, seg, status, kv_chunk);
+  if (const cudaError_t le = launch_pdl(seg_build_kernel, dim3(g.B), dim3(1024), 0, st, doc, g, seg, status, kv_chunk);
+      le != cudaSuccess) return le;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // histogram bins of the work-list sort (48 KB of shared memory at most)
   int nbins = (g.nkt > cdiv(g.L, kBwdQ) ? g.nkt : cdiv(g.L, kBwdQ)) + 1;
   if (nbins > 12288) nbins = 12288;
-  classify_kernel<<<1, 1024, static_cast<size_t>(nbins) * 4, st>>>(g, seg, nbins);
+  if (const cudaError_t le = launch_pdl(classify_kernel, dim3(1), dim3(1024), static_cast<size_t>(nbins) * 4, st, g,
+      seg, nbins); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 
