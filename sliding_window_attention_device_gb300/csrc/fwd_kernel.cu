@@ -326,8 +326,13 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
             uint32_t o[32];
             tmem_ld32(t_o + c, o);
             tmem_wait_ld();
+            const float2 av = make_float2(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), av);
+              o[e] = __float_as_uint(v.x);
+              o[e + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(t_o + c, o);
           }
           tmem_wait_st();
@@ -335,16 +340,22 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       }
       // exponent offset; -inf on a row that sees nothing of this tile, so P = 0
       const float nmm = dead ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // row sum in eight partial sums
+      // two-wide fp32 FMA and add (one instruction per pair of columns): the
+      // exponent scale * log2(e) * score - max, and the row sum in four pairs
+      // of partial sums
+      const float2 sl2v = make_float2(sl2, sl2), nmmv = make_float2(nmm, nmm);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        // exponent: scale * log2(e) * score - max in one FMA
-        const float p0 = fast_exp2(fmaf(x[2 * c], sl2, nmm)), p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, nmm));
-        rs8[c & 7] += p0 + p1;
+        const float2 ex = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), sl2v, nmmv);
+        const float p0 = fast_exp2(ex.x), p1 = fast_exp2(ex.y);
+        rs2[c & 3] = __fadd2_rn(rs2[c & 3], make_float2(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
+      const float2 r = __fadd2_rn(r01, r23);
+      const float rs = r.x + r.y;
       l += rs;
       tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
       tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
