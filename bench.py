@@ -13,10 +13,11 @@ finalize). Inputs are resident in HBM before the timed region; K/V (268 MB)
 exceed the 129 MB L2, so no flush is needed between steps.
 
 With --kv-chunks ring, each shard's K/V arrives in per-rank pieces as in a
-ring step: a forward per piece merged into the shard's (out, lse) by the
-log-sum-exp merge kernel, then one backward main per piece with the merged
-out / lse. The FLOP count is the same; the line adds the merge kernel's HBM
-roofline.
+ring step: a forward per piece merged into the shard's (out, lse) in the
+forward's epilogue, then one backward main per piece with the merged out /
+lse. --kv-chunks ring-merge does the merges with the separate log-sum-exp
+merge kernel and adds its HBM roofline to the line. The FLOP count is the
+same as the unchunked step's.
 
 With --exchange, the line is instead the sender side of the needed-only
 K/V exchange for every rank of the workload: the exchange plan built from the
@@ -266,9 +267,10 @@ class RingChunkReplica(Replica):
     contiguous K / V and dK / dV; the first chunk's forward writes the shard's
     out / lse, the others go through a scratch (out, lse) and the merge kernel."""
 
-    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None):
+    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None, fused=True):
         super().__init__(w, seed, dev, grad_dtype, ranks)
         bd = self.bd
+        self.fused = fused  # merge in the forward's epilogue (else: forward to scratch + merge kernel)
         kv_cache = {}
         self.launches_per_step = 0
         for s, sh in zip(self.shards, self.plan):
@@ -290,9 +292,10 @@ class RingChunkReplica(Replica):
             s["chunks"] = chunks
             n = len(chunks)
             # per chunk: table build + classification, forward, zero-fill + backward
-            # main; per merge one launch; per shard the backward prep (and the dq
-            # finalize for bf16 gradients)
-            self.launches_per_step += 5 * n + (n - 1) + 1 + (0 if grad_dtype == torch.float32 else 1)
+            # main; per merge one launch unless fused; per shard the backward prep
+            # (and the dq finalize for bf16 gradients)
+            self.launches_per_step += (5 * n + (0 if fused else n - 1) + 1 +
+                                       (0 if grad_dtype == torch.float32 else 1))
         self.n_merges = sum(len(s["chunks"]) - 1 for s in self.shards)
         self.kv_chunk_bytes = sum(k.numel() * 2 + v.numel() * 2 for k, v in kv_cache.values())
         self.out_c = torch.empty(w.B, w.Hq, w.L, w.D, dtype=torch.bfloat16, device=dev)
@@ -315,6 +318,9 @@ class RingChunkReplica(Replica):
         for n, c in enumerate(s["chunks"]):
             if n == 0:
                 bd.bd_attn_fwd(s["q"], c["k"], c["v"], c["seg"], c["g"], self.status, out=s["out"], lse=s["lse"])
+                continue
+            if self.fused:
+                bd.bd_attn_fwd_merge(s["q"], c["k"], c["v"], c["seg"], c["g"], self.status, s["out"], s["lse"])
                 continue
             bd.bd_attn_fwd(s["q"], c["k"], c["v"], c["seg"], c["g"], self.status, out=self.out_c, lse=self.lse_c)
             if ev is not None:
@@ -469,8 +475,11 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     w = synth.WORKLOADS[args.config]
     grad_dtype = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
     ranks = None if args.shards is None else {int(x) for x in args.shards.split(",")}
-    chunked = args.kv_chunks == "ring"
-    rep = (RingChunkReplica if chunked else Replica)(w, args.seed + rank, dev, grad_dtype, ranks)
+    chunked = args.kv_chunks in ("ring", "ring-merge")
+    if chunked:
+        rep = RingChunkReplica(w, args.seed + rank, dev, grad_dtype, ranks, fused=args.kv_chunks == "ring")
+    else:
+        rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks)
     total_flop, fwd_flop, bwd_flop = rep.flops()
 
     def barrier():
@@ -537,8 +546,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "cp_size": w.cp_size, "L": w.L, "ranks": [s["r"] for s in rep.plan], "window": w.window, "kv": w.kv,
                    "grad_dtype": args.grad_dtype, "l2": "inputs larger than L2 (K/V 268 MB), no flush",
                    "pairs": sum(s["pairs"] for s in rep.shards), "seed": args.seed,
-                   "kv_chunks": ("ring: K/V cut at the cp ranks' boundaries, owners after the shard skipped, "
-                                 f"{n_bwd} chunks, {rep.n_merges} merges per step") if chunked else "none"},
+                   "kv_chunks": (f"{args.kv_chunks}: K/V cut at the cp ranks' boundaries, owners after the shard "
+                                 f"skipped, {n_bwd} chunks, {rep.n_merges} merges per step, "
+                                 + ("in the forward's epilogue" if rep.fused else "by the merge kernel"))
+                                if chunked else "none"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
@@ -734,8 +745,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--exchange", action="store_true",
                     help="time the sender side of the needed-only K/V exchange (plan, gather, index-add) instead")
-    ap.add_argument("--kv-chunks", choices=("none", "ring"), default="none",
-                    help="ring: each shard's K/V in per-rank chunks, forward merged, backward per chunk")
+    ap.add_argument("--kv-chunks", choices=("none", "ring", "ring-merge"), default="none",
+                    help="ring: each shard's K/V in per-rank chunks, each chunk's forward merged in its epilogue, "
+                         "backward per chunk; ring-merge: the same with the separate merge kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=32,
                     help="query heads of batch row 0 in the oracle's timed CPU-baseline slice")

@@ -149,6 +149,18 @@ int bd_attn_seg_build(const int32_t* doc_ids, const bd_geom* g, void* seg, int32
 int bd_attn_seg_build_chunk(const int32_t* doc_ids, const bd_geom* g, void* seg, int32_t* status,
                             bd_stream_t stream);
 
+/* The forward over one K/V chunk merged into a running result in its
+ * epilogue (gemma4_moe.cp_local_ring: per-chunk forward and -inf-safe
+ * merge, fused): out / lse hold the running result on entry -- from
+ * bd_attn_fwd over the first chunk or from earlier calls of this one -- and
+ * the merge of it with this chunk's forward on return, by the same rule as
+ * bd_attn_merge, in fp32 before the one rounding of out to bf16. A row the
+ * chunk gives nothing keeps its running result; a row empty on both sides
+ * gets out = 0, lse = -inf; an empty running side's out is not read.
+ * Arguments, table and errors as bd_attn_fwd. */
+int bd_attn_fwd_merge(const void* q, const void* k, const void* v, const void* seg, const bd_geom* g, void* out,
+                      float* lse, int32_t* status, bd_stream_t stream);
+
 /* Log-sum-exp merge of a chunk's forward result into a running one, in place
  * (gemma4_moe.cp_local_ring: -inf-safe online softmax merge):
  *   lse = log(exp(lse) + exp(lse_chunk)),

@@ -32,7 +32,7 @@ REGIONS = ("hdr", "cu_q", "cu_k", "row_lo", "qt_krange", "kt_qrange", "full_bits
            "counts", "total")
 
 EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_seg_build_chunk",
-           "bd_attn_fwd", "bd_attn_merge",
+           "bd_attn_fwd", "bd_attn_fwd_merge", "bd_attn_merge",
            "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
            "bd_attn_bwd_finalize", "bd_attn_bwd_prep_dq", "bd_attn_bwd_main_dq",
            "bd_attn_bwd_noalloc", "bd_attn_plan_bytes", "bd_attn_plan_layout", "bd_attn_exchange_plan",
@@ -94,6 +94,8 @@ def load() -> ctypes.CDLL:
         lib.bd_attn_merge.restype = ctypes.c_int
         lib.bd_attn_fwd.argtypes = [P, P, P, P, G, P, P, P, P]
         lib.bd_attn_fwd.restype = ctypes.c_int
+        lib.bd_attn_fwd_merge.argtypes = [P, P, P, P, G, P, P, P, P]
+        lib.bd_attn_fwd_merge.restype = ctypes.c_int
         lib.bd_attn_bwd.argtypes = [P, P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
         lib.bd_attn_bwd.restype = ctypes.c_int
         lib.bd_attn_bwd_prep.argtypes = [P, P, G, P, P, P]
@@ -242,6 +244,21 @@ def bd_attn_fwd(q, k, v, seg, g: Geom, status, out=None, lse=None, stream=None):
     _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
     _check(load().bd_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(seg), ctypes.byref(g), _ptr(out), _ptr(lse),
                               _ptr(status), _stream(stream)), "bd_attn_fwd")
+    return out, lse
+
+
+def bd_attn_fwd_merge(q, k, v, seg, g: Geom, status, out, lse, stream=None):
+    """Forward over one K/V chunk merged into the running (out, lse), in place."""
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
+    _need(status, "status", torch.int32, (1,), dev)
+    _need(out, "out", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
+    _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
+    _check(load().bd_attn_fwd_merge(_ptr(q), _ptr(k), _ptr(v), _ptr(seg), ctypes.byref(g), _ptr(out), _ptr(lse),
+                                    _ptr(status), _stream(stream)), "bd_attn_fwd_merge")
     return out, lse
 
 

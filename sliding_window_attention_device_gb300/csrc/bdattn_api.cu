@@ -17,7 +17,7 @@ cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, in
 cudaError_t launch_merge(const Geom& g, void* out, float* lse, const void* out_c, const float* lse_c,
                          const int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
-                       const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
+                       const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st);
 cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
                             int32_t* status, cudaStream_t st);
 cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
@@ -253,8 +253,9 @@ int bd_attn_needed_scatter_add(const void* grad_send, const void* plan, int B, i
                                            static_cast<cudaStream_t>(stream)));
 }
 
-int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,
-                float* lse, int32_t* status, bd_stream_t stream) {
+namespace {
+int fwd_impl(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out, float* lse,
+             int32_t* status, int merge, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
   if (!q || !k || !v || !seg || !out || !lse || !status) return BD_ERR_ARG;
@@ -265,8 +266,19 @@ int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, co
   if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
       make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile))
     return BD_ERR_CUDA;
-  return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status,
+  return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status, merge,
                             static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+int bd_attn_fwd(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,
+                float* lse, int32_t* status, bd_stream_t stream) {
+  return fwd_impl(q, k, v, seg, gi, out, lse, status, 0, stream);
+}
+
+int bd_attn_fwd_merge(const void* q, const void* k, const void* v, const void* seg, const bd_geom* gi, void* out,
+                      float* lse, int32_t* status, bd_stream_t stream) {
+  return fwd_impl(q, k, v, seg, gi, out, lse, status, 1, stream);
 }
 
 }  // extern "C"

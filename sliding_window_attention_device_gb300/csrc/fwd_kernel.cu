@@ -54,7 +54,7 @@ struct FwdTmem {
   static_assert(kUsed <= 512, "tensor memory budget");
 };
 
-template <int D, int NQ, int NS>
+template <int D, int NQ, int NS, bool kMerge>
 __global__ void __launch_bounds__(128 + NQ * 128, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
@@ -114,15 +114,18 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
   const int h0 = pair * NQ, hk = h0 / g.G;
 
   if (nk == 0) {
-    // No real row in this q tile: zeros and -inf.
+    // No row of this q tile sees a key: zeros and -inf (merging: a running
+    // result is kept, an empty one set to zeros and -inf).
     if (tid >= 128) {
       const int qi = (tid - 128) >> 7, r = (tid - 128) & 127;
       const int i = qt * kTile + r;
       if (i < g.L) {
         const size_t row = (static_cast<size_t>(b) * g.Hq + h0 + qi) * g.L + i;
-        uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
-        for (int c = 0; c < D / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        lse[row] = -INFINITY;
+        if (!kMerge || lse[row] == -INFINITY) {
+          uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
+          for (int c = 0; c < D / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+          lse[row] = -INFINITY;
+        }
       }
     }
     return;
@@ -370,28 +373,57 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     } else {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      const float lse_v = (real && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      float inv = l > 0.f ? 1.0f / l : 0.f;
+      float lse_v = (real && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
       const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
       uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
+      // merging into a running (out, lse): log-sum-exp weights of the two sides;
+      // an empty side (lse -inf) has weight 0 and its out is not read
+      float w_old = 0.f;
+      bool store = i < g.L;
+      if (kMerge && store) {
+        const float lse_o = lse[row];
+        if (lse_v == -INFINITY) {
+          store = lse_o == -INFINITY;  // nothing new: keep a running result, zero an empty one
+        } else if (lse_o != -INFINITY) {
+          const float mx = fmaxf(lse_o, lse_v);
+          const float ea = expf(lse_o - mx), eb = expf(lse_v - mx), tot = ea + eb;
+          w_old = ea / tot;
+          inv *= eb / tot;
+          lse_v = mx + logf(tot);
+        }
+      }
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
         tmem_ld32(t_o + c, o);
         tmem_wait_ld();
-        if (i < g.L) {
+        if (store) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(o[8 * e + k]) * inv;
+            if (kMerge && w_old != 0.f) {
+              const uint4 old = o4[c / 8 + e];
+              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
+                v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
+                v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
+              }
+            }
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+            w.x = pack_bf16x2(v[0], v[1]);
+            w.y = pack_bf16x2(v[2], v[3]);
+            w.z = pack_bf16x2(v[4], v[5]);
+            w.w = pack_bf16x2(v[6], v[7]);
             o4[c / 8 + e] = w;
           }
         }
       }
-      if (i < g.L) lse[row] = lse_v;
+      if (store) lse[row] = lse_v;
     }
   }
 
@@ -406,9 +438,9 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
 template <int D, int NQ, int NS>
 static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                               const int32_t* seg, const Geom& g, __nv_bfloat16* out, float* lse, int32_t* status,
-                              cudaStream_t st) {
+                              int merge, cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem<D, NQ, NS>) + 1024;  // + 1 KB to align the swizzled tiles
-  auto kern = fwd_kernel<D, NQ, NS>;
+  auto kern = merge ? fwd_kernel<D, NQ, NS, true> : fwd_kernel<D, NQ, NS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);
@@ -421,18 +453,18 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
 // Two query heads of one GQA group per CTA when the group size is even and
 // D <= 128 (tensor memory: 2 x (128 + D) columns); one otherwise.
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
-                       const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st) {
+                       const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st) {
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   const bool pairs = (g.G % 2) == 0;
   switch (g.D) {
     case 64:
-      return pairs ? launch_one<64, 2, 3>(mq, mk, mv, seg, g, o, lse, status, st)
-                   : launch_one<64, 1, 3>(mq, mk, mv, seg, g, o, lse, status, st);
+      return pairs ? launch_one<64, 2, 3>(mq, mk, mv, seg, g, o, lse, status, merge, st)
+                   : launch_one<64, 1, 3>(mq, mk, mv, seg, g, o, lse, status, merge, st);
     case 128:
-      return pairs ? launch_one<128, 2, 2>(mq, mk, mv, seg, g, o, lse, status, st)
-                   : launch_one<128, 1, 2>(mq, mk, mv, seg, g, o, lse, status, st);
+      return pairs ? launch_one<128, 2, 2>(mq, mk, mv, seg, g, o, lse, status, merge, st)
+                   : launch_one<128, 1, 2>(mq, mk, mv, seg, g, o, lse, status, merge, st);
     case 256:
-      return launch_one<256, 1, 1>(mq, mk, mv, seg, g, o, lse, status, st);
+      return launch_one<256, 1, 1>(mq, mk, mv, seg, g, o, lse, status, merge, st);
     default:
       return cudaErrorInvalidValue;
   }

@@ -8,7 +8,8 @@ inside a 128-row tile, plus one chunk after the shard's rows that no row sees:
   * every chunk's forward matches oracle.fwd_chunk (rows with no key in the
     chunk: out = 0, lse = -inf);
   * merging all chunks on the GPU, from lse = -inf over a NaN-filled out,
-    matches the full-range oracle forward;
+    matches the full-range oracle forward, both with the merge kernel and
+    with the forward's merging epilogue;
   * prep once with the merged out / lse, then one backward main per chunk
     (dq accumulating, dk / dv per chunk) matches the full-range oracle backward.
 """
@@ -65,11 +66,14 @@ def test_chunked_forward_merge_and_backward(name, w, r, edges):
     else:
         extra = None
 
-    # forward per chunk, merged on the GPU
+    # forward per chunk, merged on the GPU: by the merge kernel (acc_*) and by
+    # the forward's own merging epilogue (fus_*), both from lse = -inf over a
+    # NaN-filled out
     g_full = _geom(w, c, c["kv_offset"], c["S_kv"])
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     acc_out = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
     acc_lse = torch.full((w.B, w.Hq, w.L), float("-inf"), dtype=torch.float32, device=dev)
+    fus_out, fus_lse = acc_out.clone(), acc_lse.clone()
     runs = []
     for kv_off, S_kv, lo, hi in chunks:
         runs.append((kv_off, S_kv, c["k"][:, :, lo:hi].contiguous(), c["v"][:, :, lo:hi].contiguous()))
@@ -92,6 +96,7 @@ def test_chunked_forward_merge_and_backward(name, w, r, edges):
         assert np.abs(got_lse[fin] - ref_lse[fin]).max(initial=0.0) <= LSE_ABS
         assert_close(f"{name} chunk [{kv_off},{kv_off + S_kv}) out", out, ref_out)
         bdattn.bd_attn_merge(acc_out, acc_lse, out, lse, g, status)
+        bdattn.bd_attn_fwd_merge(q, kd, vd, seg, g, status, fus_out, fus_lse)
         segs.append((g, seg, kd, vd))
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -101,6 +106,10 @@ def test_chunked_forward_merge_and_backward(name, w, r, edges):
     fin = np.isfinite(full_lse)
     assert np.abs(got_lse[fin] - full_lse[fin]).max(initial=0.0) <= LSE_ABS
     assert_close(f"{name} merged out", acc_out, full_out)
+    got_lse = fus_lse.double().cpu().numpy()
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(full_lse))
+    assert np.abs(got_lse[fin] - full_lse[fin]).max(initial=0.0) <= LSE_ABS
+    assert_close(f"{name} forward-merged out", fus_out, full_out)
 
     # backward per chunk with the merged out / lse
     ws = torch.empty(bdattn.bwd_workspace_bytes(g_full), dtype=torch.uint8, device=dev)
@@ -162,9 +171,10 @@ def test_merge_edge_cases():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key,r", [("C2", 3), ("C2", 7), ("C3", 7), ("C5w512", 5)])
-def test_ring_chunks_full_size_sampled(key, r):
-    """Full size, through the chunking and calls the benchmark's ring mode times:
+@pytest.mark.parametrize("key,r,fused", [("C2", 3, True), ("C2", 7, False), ("C3", 7, True), ("C5w512", 5, True)])
+def test_ring_chunks_full_size_sampled(key, r, fused):
+    """Full size, through the chunking and calls the benchmark's ring modes time
+    (merges in the forward's epilogue, or by the merge kernel):
     sampled rows (out, lse, dq) and keys (dk, dv) against the oracle over the
     whole K/V range; keys in a skipped block get no gradient from any row; and
     sum over all keys of dV equals the sum of dO over the real rows."""
@@ -172,7 +182,7 @@ def test_ring_chunks_full_size_sampled(key, r):
     from test_gpu_full import _oracle_sampled, _pick, _check
     w = synth.WORKLOADS[key]
     dev = torch.device("cuda")
-    rep = bench.RingChunkReplica(w, 0, dev, torch.float32, ranks={r})
+    rep = bench.RingChunkReplica(w, 0, dev, torch.float32, ranks={r}, fused=fused)
     rep.step()
     torch.cuda.synchronize()
     assert int(rep.status.item()) == 0
