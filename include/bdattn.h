@@ -27,10 +27,11 @@
  *   doc_ids  int32 [B, S_full]        0 = padding, > 0 = document id
  *   q, dout  bf16  [B, Hq,  L,    D]
  *   k, v     bf16  [B, Hkv, S_kv, D]  query head h reads kv head h / (Hq/Hkv)
+ *                                     ([S_kv, B, Hkv, D] with kv_layout = BD_KV_SBHD)
  *   out      bf16  [B, Hq,  L,    D]
  *   lse      fp32  [B, Hq,  L]        natural-log sum-exp; -inf on padding rows
  *   dq       fp32 or bf16 [B, Hq, L, D]
- *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group
+ *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group (k's layout)
  * D must be 64, 128 or 256. All device pointers are caller-owned and must be
  * 16-byte aligned. The library allocates no device memory and never
  * synchronises the stream; every entry point only enqueues work on `stream`.
@@ -67,7 +68,15 @@ typedef struct {
   int S_kv;       /* K/V buffer rows */
   int window;     /* left window W (> 0: also require p - s < W); <= 0: none */
   float scale;    /* softmax scale; <= 0 means D^-0.5 */
+  int kv_layout;  /* layout of k, v, dk, dv: BD_KV_BHSD (0) or BD_KV_SBHD (1) */
 } bd_geom;
+
+/* K/V layouts. BD_KV_SBHD is token-major, [S_kv][B][Hkv][D]: the receive
+ * buffer of the needed-only all-to-all-v (pieces in source order make the
+ * needed range), read in place; dk / dv are then written token-major too,
+ * ready to be sent back and index-added by bd_attn_needed_scatter_add. */
+#define BD_KV_BHSD 0
+#define BD_KV_SBHD 1
 
 /* Host return codes. */
 #define BD_OK 0

@@ -51,18 +51,27 @@ class Geom(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
                 ("S_full", ctypes.c_int), ("L", ctypes.c_int), ("row_offset", ctypes.c_int),
                 ("kv_offset", ctypes.c_int), ("S_kv", ctypes.c_int), ("window", ctypes.c_int),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("kv_layout", ctypes.c_int)]
 
     def __repr__(self):
         return "Geom(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
 
 
-def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=0.0) -> Geom:
+KV_BHSD, KV_SBHD = 0, 1  # K/V layouts: [B, Hkv, S_kv, D] or token-major [S_kv, B, Hkv, D]
+
+
+def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=0.0, kv_layout=KV_BHSD) -> Geom:
     """Geometry of one query shard: local rows [row_offset, row_offset+L) of a
     padded sequence of S_full positions, K/V buffer rows = positions
-    [kv_offset, kv_offset+S_kv). scale <= 0 means D**-0.5; window <= 0: none."""
+    [kv_offset, kv_offset+S_kv). scale <= 0 means D**-0.5; window <= 0: none;
+    kv_layout: KV_BHSD or KV_SBHD (token-major k, v, dk, dv)."""
     return Geom(int(B), int(Hq), int(Hkv), int(D), int(S_full), int(L), int(row_offset), int(kv_offset),
-                int(S_kv), int(window), float(scale or 0.0))
+                int(S_kv), int(window), float(scale or 0.0), int(kv_layout))
+
+
+def kv_shape(g: Geom) -> tuple:
+    """Shape of k, v, dk, dv for the geometry's K/V layout."""
+    return (g.S_kv, g.B, g.Hkv, g.D) if g.kv_layout == KV_SBHD else (g.B, g.Hkv, g.S_kv, g.D)
 
 
 _lock = threading.Lock()
@@ -232,8 +241,8 @@ def bd_attn_fwd(q, k, v, seg, g: Geom, status, out=None, lse=None, stream=None):
     """out [B,Hq,L,D] bf16 and lse [B,Hq,L] fp32 (natural log; -inf on padding rows)."""
     dev = q.device
     _need(q, "q", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
-    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(k, "k", torch.bfloat16, kv_shape(g), dev)
+    _need(v, "v", torch.bfloat16, kv_shape(g), dev)
     _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
     _need(status, "status", torch.int32, (1,), dev)
     if out is None:
@@ -251,8 +260,8 @@ def bd_attn_fwd_merge(q, k, v, seg, g: Geom, status, out, lse, stream=None):
     """Forward over one K/V chunk merged into the running (out, lse), in place."""
     dev = q.device
     _need(q, "q", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
-    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(k, "k", torch.bfloat16, kv_shape(g), dev)
+    _need(v, "v", torch.bfloat16, kv_shape(g), dev)
     _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
     _need(status, "status", torch.int32, (1,), dev)
     _need(out, "out", torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
@@ -270,22 +279,22 @@ def bd_attn_bwd(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.
         raise ValueError("grad_dtype must be torch.float32 or torch.bfloat16")
     for name, t in (("dout", dout), ("q", q), ("out", out)):
         _need(t, name, torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
-    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(k, "k", torch.bfloat16, kv_shape(g), dev)
+    _need(v, "v", torch.bfloat16, kv_shape(g), dev)
     _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
     _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
     _need(status, "status", torch.int32, (1,), dev)
     if dq is None:
         dq = torch.empty(g.B, g.Hq, g.L, g.D, dtype=grad_dtype, device=dev)
     if dk is None:
-        dk = torch.empty(g.B, g.Hkv, g.S_kv, g.D, dtype=grad_dtype, device=dev)
+        dk = torch.empty(kv_shape(g), dtype=grad_dtype, device=dev)
     if dv is None:
-        dv = torch.empty(g.B, g.Hkv, g.S_kv, g.D, dtype=grad_dtype, device=dev)
+        dv = torch.empty(kv_shape(g), dtype=grad_dtype, device=dev)
     if workspace is None:
         workspace = torch.empty(bwd_workspace_bytes(g), dtype=torch.uint8, device=dev)
     _need(dq, "dq", grad_dtype, (g.B, g.Hq, g.L, g.D), dev)
-    _need(dk, "dk", grad_dtype, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(dv, "dv", grad_dtype, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(dk, "dk", grad_dtype, kv_shape(g), dev)
+    _need(dv, "dv", grad_dtype, kv_shape(g), dev)
     _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
     code = BD_DTYPE_BF16 if grad_dtype == torch.bfloat16 else BD_DTYPE_F32
     _check(load().bd_attn_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seg),
@@ -313,12 +322,12 @@ def bd_attn_bwd_main(dout, q, k, v, lse, seg, g: Geom, status, workspace, dk, dv
         raise ValueError("dk / dv must be float32 or bfloat16")
     for name, t in (("dout", dout), ("q", q)):
         _need(t, name, torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
-    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(k, "k", torch.bfloat16, kv_shape(g), dev)
+    _need(v, "v", torch.bfloat16, kv_shape(g), dev)
     _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
     _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
-    _need(dk, "dk", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(dv, "dv", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(dk, "dk", gd, kv_shape(g), dev)
+    _need(dv, "dv", gd, kv_shape(g), dev)
     _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
     _need(status, "status", torch.int32, (1,), dev)
     code = BD_DTYPE_BF16 if gd == torch.bfloat16 else BD_DTYPE_F32
@@ -360,13 +369,13 @@ def bd_attn_bwd_main_dq(dout, q, k, v, lse, seg, g: Geom, status, workspace, dq,
         raise ValueError("dk / dv must be float32 or bfloat16")
     for name, t in (("dout", dout), ("q", q)):
         _need(t, name, torch.bfloat16, (g.B, g.Hq, g.L, g.D), dev)
-    _need(k, "k", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(v, "v", torch.bfloat16, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(k, "k", torch.bfloat16, kv_shape(g), dev)
+    _need(v, "v", torch.bfloat16, kv_shape(g), dev)
     _need(lse, "lse", torch.float32, (g.B, g.Hq, g.L), dev)
     _need(seg, "seg", torch.int32, (seg_bytes(g) // 4,), dev)
     _need(dq, "dq", torch.float32, (g.B, g.Hq, g.L, g.D), dev)
-    _need(dk, "dk", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
-    _need(dv, "dv", gd, (g.B, g.Hkv, g.S_kv, g.D), dev)
+    _need(dk, "dk", gd, kv_shape(g), dev)
+    _need(dv, "dv", gd, kv_shape(g), dev)
     _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
     _need(status, "status", torch.int32, (1,), dev)
     code = BD_DTYPE_BF16 if gd == torch.bfloat16 else BD_DTYPE_F32

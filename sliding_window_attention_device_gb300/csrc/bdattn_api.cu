@@ -91,6 +91,7 @@ int to_geom(const bd_geom* in, Geom* g) {
   if (static_cast<long long>(in->B) * (in->L + 1) * 4 + static_cast<long long>(in->B) * in->S_kv > (1LL << 29))
     return BD_ERR_ARG;
   if (!(in->scale == in->scale)) return BD_ERR_ARG;  // NaN
+  if (in->kv_layout != BD_KV_BHSD && in->kv_layout != BD_KV_SBHD) return BD_ERR_ARG;
   g->B = in->B;
   g->Hq = in->Hq;
   g->Hkv = in->Hkv;
@@ -103,6 +104,7 @@ int to_geom(const bd_geom* in, Geom* g) {
   g->S_kv = in->S_kv;
   g->window = in->window > 0 ? in->window : 0;
   g->scale = in->scale > 0.f ? in->scale : 1.0f / std::sqrt(static_cast<float>(in->D));
+  g->kv_tm = in->kv_layout == BD_KV_SBHD;
   seg_layout(g->B, g->L, g->S_kv, g->off, &g->nqt, &g->nkt, &g->nkw);
   return BD_OK;
 }
@@ -113,6 +115,23 @@ int make_map(CUtensorMap* m, const void* ptr, int D, int rows, int planes, int b
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(rows) * D * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BD_OK : BD_ERR_CUDA;
+}
+
+// K or V: the map above over [B*Hkv][S_kv][D], or, token-major
+// ([S_kv][B*Hkv][D]), dims (D, B*Hkv, S_kv) with a (64 x 1 x box_rows) box --
+// the same shared-memory tile, loaded at coordinates (d, plane, row) instead
+// of (d, row, plane); rows past S_kv read as zero either way.
+int make_map_kv(CUtensorMap* m, const void* ptr, const Geom& g, int box_rows) {
+  if (!g.kv_tm) return make_map(m, ptr, g.D, g.S_kv, g.B * g.Hkv, box_rows);
+  const cuuint64_t planes = static_cast<cuuint64_t>(g.B) * g.Hkv;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(g.D), planes, static_cast<cuuint64_t>(g.S_kv)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.D) * 2, planes * g.D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -263,8 +282,8 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* seg, const
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
   CUtensorMap mq, mk, mv;
-  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
-      make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile))
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map_kv(&mk, k, g, kTile) ||
+      make_map_kv(&mv, v, g, kTile))
     return BD_ERR_CUDA;
   return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status, merge,
                             static_cast<cudaStream_t>(stream)));
@@ -313,7 +332,7 @@ int bwd_main_impl(const void* dout, const void* q, const void* k, const void* v,
   CUtensorMap mq, mdo, mk, mv, mdq;
   const int qbox = bwd_q_box_rows(g.D);
   if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, qbox) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, qbox) ||
-      make_map(&mk, k, g.D, g.S_kv, g.B * g.Hkv, kTile) || make_map(&mv, v, g.D, g.S_kv, g.B * g.Hkv, kTile) ||
+      make_map_kv(&mk, k, g, kTile) || make_map_kv(&mv, v, g, kTile) ||
       make_map_f32(&mdq, workspace, g.D, g.L, g.B * g.Hq))
     return BD_ERR_CUDA;
   return cuda_rc(launch_bwd_main(mq, mdo, mk, mv, mdq, static_cast<const int32_t*>(seg), g, lse, dk, dv,

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = s.b, kt = s.kt, q_lo = s.q_lo, nq = s.nq, n_real = s.n_real;
   const int G = g.G;
   const int n_it = G * nq;  // iteration it: query head hk*G + it / nq, q tile q_lo + it % nq
-  const size_t kv_row0 = (static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv;
+  // dK / dV row j of this (batch row, kv head): kv_row(g, b, hk, j)
   const bool is_pds = (warp >= 4 && warp < 8) || warp >= 12;
   const int half = warp >= 12 ? 1 : 0;
 
@@ -195,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&s.kv_full, 2 * kChunks * kChunk);
       for (int c = 0; c < kChunks; ++c) {
-        tma_load_3d(t.k[c], &tm_k, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
-        tma_load_3d(t.v[c], &tm_v, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
+        tma_load_3d(t.k[c], &tm_k, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
+        tma_load_3d(t.v[c], &tm_v, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
       }
     }
     int issued = 0, gq = 0, qt = 0;  // (head, q tile) of iteration `it`
@@ -443,14 +443,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < g.S_kv) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);
-            store_row(dv, (kv_row0 + j) * D + c, f);
+            store_row(dv, kv_row(g, b, hk, j) * D + c, f);
           }
           tmem_ld32(tbase + lane_off + kColDk + c, vv);
           tmem_wait_ld();
           if (j < g.S_kv) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
-            store_row(dk, (kv_row0 + j) * D + c, f);
+            store_row(dk, kv_row(g, b, hk, j) * D + c, f);
           }
         }
       }

@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int G = g.G;
   const int n_it_pass = G * nq64;
   const int n_it = kPasses * n_it_pass;
-  const size_t kv_row0 = (static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv;
+  // dK / dV row j of this (batch row, kv head): kv_row(g, b, hk, j)
   // P / dS warpgroups: warps 4-7 (half 0, q columns 0-31) and 12-15 (half 1, 32-63)
   const bool is_pds = (warp >= 4 && warp < 8) || warp >= 12;
   const int half = warp >= 12 ? 1 : 0;
@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&s.kv_full, 2 * kChunks * Smem::kKChunk);
       for (int c = 0; c < kChunks; ++c) {
-        tma_load_3d(s.k[c], &tm_k, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
-        tma_load_3d(s.v[c], &tm_v, &s.kv_full, c * 64, kt * kTile, b * g.Hkv + hk);
+        tma_load_3d(s.k[c], &tm_k, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
+        tma_load_3d(s.v[c], &tm_v, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
       }
     }
     int issued = 0;
@@ -532,14 +532,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (j < g.S_kv) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);
-            store_row(dv, (kv_row0 + j) * D + pass * kDp + c, f);
+            store_row(dv, kv_row(g, b, hk, j) * D + pass * kDp + c, f);
           }
           tmem_ld32(tbase + lane_off + Cfg::kColDk + c, vv);
           tmem_wait_ld();
           if (j < g.S_kv) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
-            store_row(dk, (kv_row0 + j) * D + pass * kDp + c, f);
+            store_row(dk, kv_row(g, b, hk, j) * D + pass * kDp + c, f);
           }
         }
         tc_fence_before();

@@ -17,6 +17,7 @@ struct Geom {
   int B, Hq, Hkv, D, G;
   int S_full, L, row_offset, kv_offset, S_kv, window;
   float scale;
+  int kv_tm;                      // k, v, dk, dv token-major: [S_kv][B][Hkv][D]
   int nqt, nkt, nkw;              // 128-row q tiles, 128-row K/V tiles, bitmap words per q tile
   int off[BD_SEG_NOFF];           // word offsets of the table regions
 };
@@ -41,6 +42,12 @@ __host__ __device__ inline void seg_layout(int B, int L, int S_kv, int* off, int
   off[BD_SEG_OFF_BWD_WORK] = o;   o = align4(o + B * (*nkt));
   off[BD_SEG_OFF_COUNTS] = o;     o = align4(o + 8);
   off[BD_SEG_OFF_TOTAL] = o;
+}
+
+// Row index of (batch row b, kv head hk, K/V buffer row j) in k, v, dk, dv.
+__host__ __device__ inline size_t kv_row(const Geom& g, int b, int hk, int j) {
+  return g.kv_tm ? (static_cast<size_t>(j) * g.B + b) * g.Hkv + hk
+                 : (static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv + j;
 }
 
 // Exchange plan layout (BD_PLAN_OFF_* regions, each on a 16-byte boundary).
@@ -136,13 +143,22 @@ __device__ inline void zero_unattended_kv(const int32_t* seg, const Geom& g, int
     }
     const int b = wi / g.nkt, r0 = (wi % g.nkt) * kTile;
     const int r1 = r0 + kTile < g.S_kv ? r0 + kTile : g.S_kv;
-    const size_t off = ((static_cast<size_t>(b) * g.Hkv + hk) * g.S_kv + r0) * row_bytes;
-    const size_t n16 = static_cast<size_t>(r1 - r0) * row_bytes / 16;
-    uint4* pk = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dk) + off);
-    uint4* pv = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dv) + off);
-    for (size_t i = t; i < n16; i += nthr) {
-      __stcs(pk + i, zero);
-      __stcs(pv + i, zero);
+    const size_t vpr = row_bytes / 16;  // 16-byte pieces per row
+    const size_t n16 = static_cast<size_t>(r1 - r0) * vpr;
+    uint4* pk = static_cast<uint4*>(dk);
+    uint4* pv = static_cast<uint4*>(dv);
+    if (!g.kv_tm) {  // the tile's rows are contiguous
+      const size_t off = kv_row(g, b, hk, r0) * vpr;
+      for (size_t i = t; i < n16; i += nthr) {
+        __stcs(pk + off + i, zero);
+        __stcs(pv + off + i, zero);
+      }
+    } else {  // token-major: one row of this kv head per token
+      for (size_t i = t; i < n16; i += nthr) {
+        const size_t off = kv_row(g, b, hk, r0 + static_cast<int>(i / vpr)) * vpr + i % vpr;
+        __stcs(pk + off, zero);
+        __stcs(pv + off, zero);
+      }
     }
   }
 }

@@ -156,13 +156,13 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         break;
       mbar_arrive_expect_tx(&s.k_full[st], kChunks * Smem::kChunkBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_3d(s.k[st][c], &tm_k, &s.k_full[st], c * 64, (kt_lo + j) * kTile, b * g.Hkv + hk);
+        tma_load_3d(s.k[st][c], &tm_k, &s.k_full[st], c * 64, g.kv_tm ? b * g.Hkv + hk : (kt_lo + j) * kTile, g.kv_tm ? (kt_lo + j) * kTile : b * g.Hkv + hk);
       ++k_issued;
       if (j >= NS && !pipe_wait(&s.v_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
         break;
       mbar_arrive_expect_tx(&s.v_full[st], kChunks * Smem::kChunkBytes);
       for (int c = 0; c < kChunks; ++c)
-        tma_load_3d(s.v[st][c], &tm_v, &s.v_full[st], c * 64, (kt_lo + j) * kTile, b * g.Hkv + hk);
+        tma_load_3d(s.v[st][c], &tm_v, &s.v_full[st], c * 64, g.kv_tm ? b * g.Hkv + hk : (kt_lo + j) * kTile, g.kv_tm ? (kt_lo + j) * kTile : b * g.Hkv + hk);
       ++v_issued;
     }
     if (v_issued < nk) {

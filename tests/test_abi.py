@@ -106,3 +106,16 @@ def test_plan_constants_and_layout(lib):
     assert bdattn.plan_bytes(B, W, L) == 4 * lay["total"]
     assert lib.bd_attn_plan_bytes(0, 8, 100) == 0 and lib.bd_attn_plan_bytes(1, 1025, 4) == 0
     assert lib.bd_attn_exchange_plan(None, 1, 64, 4, 0, None, None, None) == bdattn.BD_ERR_ARG
+
+
+def test_kv_layout_constants_and_validation(lib):
+    text = open(HEADER).read()
+    consts = dict(re.findall(r"#define\s+(BD_KV_\w+)\s+(\d+)", text))
+    assert int(consts["BD_KV_BHSD"]) == bdattn.KV_BHSD and int(consts["BD_KV_SBHD"]) == bdattn.KV_SBHD
+    fields = re.search(r"typedef struct \{(.*?)\} bd_geom;", text, re.S).group(1)
+    names = re.findall(r"\b(?:int|float)\s+(\w+);", fields)
+    assert names == [n for n, _ in bdattn.Geom._fields_]
+    g = bdattn.geom(1, 2, 1, 64, 256, 64, 0, 0, 256, 0, kv_layout=bdattn.KV_SBHD)
+    assert bdattn.kv_shape(g) == (256, 1, 1, 64) and lib.bd_attn_seg_bytes(ctypes.byref(g)) > 0
+    g.kv_layout = 2
+    assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
