@@ -183,9 +183,11 @@ def kernel_source_sha() -> str:
 class Replica:
     """Device-resident inputs / outputs of every shard of the workload."""
 
-    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None):
+    def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None,
+                 deterministic=False):
         from sliding_window_attention_device_gb300 import bdattn
         self.bd, self.w, self.dev, self.grad_dtype = bdattn, w, dev, grad_dtype
+        self.deterministic = deterministic  # dq by the fixed-order pass: bitwise reproducible
         self.doc_np = synth.doc_layout(w.layout, w.B, w.S, seed)
         self.plan = [sh for sh in shard_plan(w, self.doc_np) if ranks is None or sh["r"] in ranks]
         self.doc = torch.from_numpy(self.doc_np).to(dev)
@@ -214,6 +216,8 @@ class Replica:
         # zero-fill of unattended dK / dV + backward main, and (bf16 gradients
         # only) the dq finalize; fp32 dq is accumulated in place
         self.launches_per_step = (6 if grad_dtype == torch.float32 else 7) * len(self.shards)
+        if deterministic:  # delta, zero-fill, dK / dV, dq: one more launch per shard than the fp32 path
+            self.launches_per_step = 7 * len(self.shards)
 
     def flops(self) -> tuple[float, float, float]:
         D, Hq = self.w.D, self.w.Hq
@@ -232,6 +236,15 @@ class Replica:
         bd.bd_attn_fwd(s["q"], s["k"], s["v"], s["seg"], g, self.status, out=s["out"], lse=s["lse"])
         if ev is not None:
             ev["fwd"][i][1].record()
+        if self.deterministic:
+            if ev is not None:
+                ev["bwd"][i][0].record()
+            bd.bd_attn_bwd_deterministic(s["do"], s["q"], s["k"], s["v"], s["out"], s["lse"], s["seg"], g,
+                                         self.status, grad_dtype=s["dq"].dtype, dq=s["dq"], dk=s["dk"], dv=s["dv"],
+                                         workspace=ws)
+            if ev is not None:
+                ev["bwd"][i][1].record()
+            return
         direct = s["dq"].dtype == torch.float32  # fp32 dq is its own accumulator: no finalize
         if direct:
             bd.bd_attn_bwd_prep_dq(s["do"], s["out"], g, self.status, ws, s["dq"])
@@ -479,7 +492,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if chunked:
         rep = RingChunkReplica(w, args.seed + rank, dev, grad_dtype, ranks, fused=args.kv_chunks == "ring")
     else:
-        rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks)
+        rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks, deterministic=args.deterministic)
     total_flop, fwd_flop, bwd_flop = rep.flops()
 
     def barrier():
@@ -534,7 +547,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     traffic = None
-    if TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked:
+    if (TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked
+            and not getattr(rep, "deterministic", False)):
         traffic = TRAFFIC["bytes_per_launch"]  # measured per whole-shard launch, not per chunk
     n_bwd = sum(len(s["chunks"]) for s in rep.shards) if chunked else len(rep.shards)
     fwd_kernel_ms = fwd_ms - merge_ms  # the forward region less its merges
@@ -546,6 +560,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                    "cp_size": w.cp_size, "L": w.L, "ranks": [s["r"] for s in rep.plan], "window": w.window, "kv": w.kv,
                    "grad_dtype": args.grad_dtype, "l2": "inputs larger than L2 (K/V 268 MB), no flush",
                    "pairs": sum(s["pairs"] for s in rep.shards), "seed": args.seed,
+                   "backward": "deterministic (fixed-order dq pass)" if getattr(rep, "deterministic", False)
+                   else "dq by fp32 atomic additions",
                    "kv_chunks": (f"{args.kv_chunks}: K/V cut at the cp ranks' boundaries, owners after the shard "
                                  f"skipped, {n_bwd} chunks, {rep.n_merges} merges per step, "
                                  + ("in the forward's epilogue" if rep.fused else "by the merge kernel"))
@@ -554,7 +570,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
-        "roofline": {"kernel": "bwd128_kernel<128> (backward main stage, with its dK/dV zero-fill launch)", "bound": "tensor", "achieved": round(bwd_achieved, 2),
+        "roofline": {"kernel": ("backward: delta, zero-fill, bwd128_kernel<128> without dq, bwd_dq_kernel<128>"
+                                if getattr(rep, "deterministic", False) else
+                                "bwd128_kernel<128> (backward main stage, with its dK/dV zero-fill launch)"),
+                     "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
                      "traffic": traffic,
@@ -743,6 +762,8 @@ def main():
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32")
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="bitwise reproducible backward (dq by a fixed-order pass instead of atomic additions)")
     ap.add_argument("--exchange", action="store_true",
                     help="time the sender side of the needed-only K/V exchange (plan, gather, index-add) instead")
     ap.add_argument("--kv-chunks", choices=("none", "ring", "ring-merge"), default="none",

@@ -208,6 +208,18 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
                 const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk, void* dv, void* workspace,
                 int32_t* status, bd_stream_t stream);
 
+/* The same backward with bitwise reproducible results (the pages'
+ * `_CP_FLASH_DETERMINISTIC`): dk / dv as bd_attn_bwd (they accumulate inside
+ * one CTA), and dq from a separate pass in which one CTA per 128-row q tile and
+ * query head walks its K/V tiles in increasing order, recomputing S and dP and
+ * accumulating dQ in tensor memory -- no atomic additions anywhere. Same
+ * arguments and results as bd_attn_bwd (workspace: the same size, holding
+ * delta); D must be 64 or 128 (BD_ERR_ARG otherwise). Three launches: delta,
+ * zero-fill + dK / dV, dq. */
+int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                              const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq,
+                              void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream);
+
 /* The three stages bd_attn_bwd runs, one kernel each, for callers that want
  * to schedule or time them separately (same arguments, same rules):
  *  _prep:     delta[B,Hq,L] = rowsum(dout * out) in fp32 and a zeroed fp32 dq

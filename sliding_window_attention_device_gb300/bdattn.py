@@ -33,7 +33,8 @@ REGIONS = ("hdr", "cu_q", "cu_k", "row_lo", "qt_krange", "kt_qrange", "full_bits
 
 EXPORTS = ("bd_attn_seg_bytes", "bd_attn_seg_layout", "bd_attn_seg_build", "bd_attn_seg_build_chunk",
            "bd_attn_fwd", "bd_attn_fwd_merge", "bd_attn_merge",
-           "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_prep", "bd_attn_bwd_main",
+           "bd_attn_bwd_workspace_bytes", "bd_attn_bwd", "bd_attn_bwd_deterministic", "bd_attn_bwd_prep",
+           "bd_attn_bwd_main",
            "bd_attn_bwd_finalize", "bd_attn_bwd_prep_dq", "bd_attn_bwd_main_dq",
            "bd_attn_bwd_noalloc", "bd_attn_plan_bytes", "bd_attn_plan_layout", "bd_attn_exchange_plan",
            "bd_attn_needed_gather", "bd_attn_needed_scatter_add", "bd_attn_strerror",
@@ -107,6 +108,8 @@ def load() -> ctypes.CDLL:
         lib.bd_attn_fwd_merge.restype = ctypes.c_int
         lib.bd_attn_bwd.argtypes = [P, P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
         lib.bd_attn_bwd.restype = ctypes.c_int
+        lib.bd_attn_bwd_deterministic.argtypes = [P, P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P, P]
+        lib.bd_attn_bwd_deterministic.restype = ctypes.c_int
         lib.bd_attn_bwd_prep.argtypes = [P, P, G, P, P, P]
         lib.bd_attn_bwd_prep.restype = ctypes.c_int
         lib.bd_attn_bwd_main.argtypes = [P, P, P, P, P, P, G, ctypes.c_int, P, P, P, P, P]
@@ -272,7 +275,7 @@ def bd_attn_fwd_merge(q, k, v, seg, g: Geom, status, out, lse, stream=None):
 
 
 def bd_attn_bwd(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.float32, dq=None, dk=None,
-                dv=None, workspace=None, stream=None):
+                dv=None, workspace=None, stream=None, _fn="bd_attn_bwd"):
     """dq [B,Hq,L,D], dk / dv [B,Hkv,S_kv,D] (summed over each GQA group) in grad_dtype."""
     dev = q.device
     if grad_dtype not in (torch.float32, torch.bfloat16):
@@ -297,10 +300,17 @@ def bd_attn_bwd(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.
     _need(dv, "dv", grad_dtype, kv_shape(g), dev)
     _need(workspace, "workspace", torch.uint8, (bwd_workspace_bytes(g),), dev)
     code = BD_DTYPE_BF16 if grad_dtype == torch.bfloat16 else BD_DTYPE_F32
-    _check(load().bd_attn_bwd(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seg),
-                              ctypes.byref(g), code, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _ptr(status),
-                              _stream(stream)), "bd_attn_bwd")
+    _check(getattr(load(), _fn)(_ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(seg),
+                                ctypes.byref(g), code, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _ptr(status),
+                                _stream(stream)), _fn)
     return dq, dk, dv
+
+
+def bd_attn_bwd_deterministic(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.float32, dq=None,
+                              dk=None, dv=None, workspace=None, stream=None):
+    """bd_attn_bwd with bitwise reproducible results (dq by a fixed-order pass; D = 64 or 128)."""
+    return bd_attn_bwd(dout, q, k, v, out, lse, seg, g, status, grad_dtype, dq, dk, dv, workspace, stream,
+                       _fn="bd_attn_bwd_deterministic")
 
 
 def bd_attn_bwd_prep(dout, out, g: Geom, status, workspace, stream=None):

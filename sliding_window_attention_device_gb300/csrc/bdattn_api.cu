@@ -26,6 +26,15 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
 cudaError_t launch_bwd_finalize(const Geom& g, void* dq, int bf16, void* workspace, int32_t* status,
                                 cudaStream_t st);
 size_t bwd_workspace_bytes(const Geom& g);
+cudaError_t launch_bwd_delta(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
+                             cudaStream_t st);
+const float* bwd_delta_ptr(const Geom& g, void* workspace);
+cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                                 void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st);
+cudaError_t launch_bwd_dq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                          const float* delta, void* dq, int bf16, int32_t* status, cudaStream_t st);
 cudaError_t launch_exchange_plan(const int32_t* doc, int B, int S, int W, int rank, int32_t* plan, int32_t* status,
                                  cudaStream_t st);
 cudaError_t launch_needed_gather(const void* x, const int32_t* plan, int B, int C, int L, int vshift, void* send,
@@ -377,6 +386,33 @@ int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* work
   if (int rc = check_device()) return rc;
   return cuda_rc(launch_bwd_finalize(g, dq, grad_dtype == BD_DTYPE_BF16, workspace, status,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, const void* v, const void* out,
+                              const float* lse, const void* seg, const bd_geom* gi, int grad_dtype, void* dq,
+                              void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream) {
+  Geom g;
+  if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D != 64 && g.D != 128) return BD_ERR_ARG;
+  if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
+    return BD_ERR_ARG;
+  if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
+  if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(seg) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return BD_ERR_ARG;
+  if (int rc = check_device()) return rc;
+  if (!load_encode()) return BD_ERR_CUDA;
+  CUtensorMap mq, mdo, mk, mv;
+  if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kTile) ||
+      make_map_kv(&mk, k, g, kTile) || make_map_kv(&mv, v, g, kTile))
+    return BD_ERR_CUDA;
+  const auto st = static_cast<cudaStream_t>(stream);
+  const int32_t* sg = static_cast<const int32_t*>(seg);
+  const int bf16 = grad_dtype == BD_DTYPE_BF16;
+  if (int rc = cuda_rc(launch_bwd_delta(g, dout, out, workspace, status, st))) return rc;
+  if (int rc = cuda_rc(launch_bwd_main_nodq(mq, mdo, mk, mv, sg, g, lse, dk, dv, bf16, workspace, status, st)))
+    return rc;
+  return cuda_rc(launch_bwd_dq(mq, mdo, mk, mv, sg, g, lse, bwd_delta_ptr(g, workspace), dq, bf16, status, st));
 }
 
 int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* out, const float* lse,

@@ -76,7 +76,9 @@ __host__ __device__ constexpr size_t bwd128_smem_bytes() {
   return sizeof(Tiles<D>) + sizeof(Ctl);
 }
 
-template <int D>
+// kDq: also the dq products and their reductions (else dK / dV only, for a
+// separate deterministic dq pass)
+template <int D, bool kDq>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -295,11 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ^T = K^T dS^T into the dP^T columns (dS is written, so dP^T was read)
         if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
         tc_fence_after();
+        if constexpr (kDq) {
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ss(tbase + kColDp, desc_at(dMN, a_k + ks * 2048), desc_at(dMN, a_ds + ks * 2048), idDQ,
-                  ks > 0 ? 1u : 0u);
-        umma_commit(&s.dq_full);
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_ss(tbase + kColDp, desc_at(dMN, a_k + ks * 2048), desc_at(dMN, a_ds + ks * 2048), idDQ,
+                    ks > 0 ? 1u : 0u);
+          umma_commit(&s.dq_full);
+        }
         // dK += dS^T Q
 #pragma unroll
         for (int ks = 0; ks < kQ / 16; ++ks)
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 == n_it) umma_commit(&s.acc_full);
         // dP^T of the next tile once dQ^T has been read out of those columns
         if (it + 1 < n_it) {
-          if (!wait(&s.dq_empty, it & 1)) { ok = false; break; }
+          if (kDq && !wait(&s.dq_empty, it & 1)) { ok = false; break; }
           tc_fence_after();
           issue_t(kColDp, a_v, a_do + (st ^ 1) * kStage);
           umma_commit(&s.dp_full);
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -532,7 +536,7 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   if (e != cudaSuccess) return e;
   const size_t smem = need + 1024 <= static_cast<size_t>(max_optin) ? need + 1024 : static_cast<size_t>(max_optin);
   if (smem < need) return cudaErrorInvalidValue;
-  auto kern = bwd128_kernel<D>;
+  auto kern = dq_acc ? bwd128_kernel<D, true> : bwd128_kernel<D, false>;  // no accumulator: dK / dV only
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // only tiles some local row can reach by position get a working CTA; with

@@ -40,7 +40,8 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 }
 
 // ----------------------------------------------------------------- K4a
-// delta[row] = sum_d dout[row, d] * out[row, d] (fp32) and dq_acc[row, :] = 0.
+// delta[row] = sum_d dout[row, d] * out[row, d] (fp32) and, given an
+// accumulator, dq_acc[row, :] = 0.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ dout,
                                                       const __nv_bfloat16* __restrict__ out,
@@ -68,9 +69,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 #pragma unroll
     for (int o = kLanes / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, kLanes);
     if (part == 0) delta[row] = acc;
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc) {  // none: delta only (the fixed-order dq pass writes dq itself)
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -687,12 +690,30 @@ static float* ws_delta(const Geom& g, void* workspace) {
 
 // K4a: delta (in the workspace) and a zeroed dq accumulator: `dq_f32` when
 // given (the fp32 dq output itself), else the workspace's.
+namespace {
+cudaError_t launch_pre(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_acc,
+                       int32_t* status, cudaStream_t st);
+}  // namespace
+
 cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
                             int32_t* status, cudaStream_t st) {
+  return launch_pre(g, dout, out, workspace, dq_f32 ? dq_f32 : static_cast<float*>(workspace), status, st);
+}
+
+// delta only, for the fixed-order dq pass
+cudaError_t launch_bwd_delta(const Geom& g, const void* dout, const void* out, void* workspace, int32_t* status,
+                             cudaStream_t st) {
+  return launch_pre(g, dout, out, workspace, nullptr, status, st);
+}
+
+const float* bwd_delta_ptr(const Geom& g, void* workspace) { return ws_delta(g, workspace); }
+
+namespace {
+cudaError_t launch_pre(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_acc,
+                       int32_t* status, cudaStream_t st) {
   const long long rows = static_cast<long long>(g.B) * g.Hq * g.L;
   const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
   const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(out);
-  float* dq_acc = dq_f32 ? dq_f32 : static_cast<float*>(workspace);
   float* delta = ws_delta(g, workspace);
   const unsigned grid = grid_for(rows * (g.D / 8));
   switch (g.D) {
@@ -706,6 +727,7 @@ cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, vo
   }
   return cudaGetLastError();
 }
+}  // namespace
 
 cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
@@ -740,6 +762,20 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
       return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// K4 without the dq products (D = 64 / 128): dK, dV and the zero-fill only,
+// for the fixed-order dq pass.
+cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                                 const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                                 void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
+  if (g.D != 64 && g.D != 128) return cudaErrorInvalidValue;
+  const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
+  const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
+  if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
+      status); le != cudaSuccess) return le;
+  return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
+                            st);
 }
 
 // K4b: dq = the accumulator (already scaled) in the gradient dtype.

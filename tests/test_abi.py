@@ -119,3 +119,9 @@ def test_kv_layout_constants_and_validation(lib):
     assert bdattn.kv_shape(g) == (256, 1, 1, 64) and lib.bd_attn_seg_bytes(ctypes.byref(g)) > 0
     g.kv_layout = 2
     assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
+
+
+def test_deterministic_backward_rejects_d256(lib):
+    g = bdattn.geom(1, 2, 1, 256, 256, 64, 0, 0, 256, 0)
+    assert lib.bd_attn_bwd_deterministic(None, None, None, None, None, None, None, ctypes.byref(g), 0, None, None,
+                                         None, None, None, None) == bdattn.BD_ERR_ARG
