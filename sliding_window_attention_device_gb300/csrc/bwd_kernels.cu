@@ -139,9 +139,12 @@ struct BwdSmem {
   alignas(1024) uint8_t dout[NSQ][kChunks][kQChunk];
   alignas(1024) uint8_t ds[kKChunk];  // dS^T, 128 keys x 64 q, bf16, 128B-swizzled
   DqStage<BwdCfg<D>::kStageSlots> stage;
-  alignas(16) float lse2[NSQ][kBwdQ];  // per q row: lse * log2(e)
-  alignas(16) float delta[NSQ][kBwdQ];
-  uint64_t kv_full, q_full[NSQ], q_empty[NSQ];
+  alignas(16) float lse2[2][kBwdQ];  // per q row: lse * log2(e), by tile parity
+  alignas(16) float delta[2][kBwdQ];
+  // the Q / dO stage in two groups (chunks [g kDp/64, (g+1) kDp/64) of both):
+  // a tile frees the group its dK / dV products do not read as soon as its S
+  // and dP products are done, so the next tile's copy of it starts early
+  uint64_t kv_full, grp_full[2], grp_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -163,6 +166,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   pdl_begin();
   using Cfg = BwdCfg<D>;
   constexpr int NSQ = Cfg::kNsq, kDp = Cfg::kDp, kPasses = Cfg::kPasses;
+  static_assert(NSQ == 1 && kPasses == 2, "one Q / dO stage in two groups, two passes over D (D = 256)");
+  constexpr int kGrp = kDp / 64;  // 64-column chunks per group
   using Smem = BwdSmem<D, NSQ>;
   constexpr int kChunks = Smem::kChunks;
   extern __shared__ uint8_t smem_raw[];
@@ -209,9 +214,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     s.skip = (!ok || *vstatus != 0) ? 1 : 0;
     s.abort_flag = 0;
     mbar_init(&s.kv_full, 1);
-    for (int i = 0; i < NSQ; ++i) {
-      mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.grp_full[i], 1);
+      mbar_init(&s.grp_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
     mbar_init(&s.dp_full, 1);
@@ -288,9 +293,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(s.v[c], &tm_v, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
       }
     }
-    int issued = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % NSQ, n = it / NSQ;
+    int issued[2] = {0, 0};
+    bool stopped = false;
+    for (int it = 0; it < n_it && !stopped; ++it) {
       int pass, h, q0;
       decode(it, pass, h, q0);
       // the per-row values are fetched before waiting for the free stage so
@@ -307,31 +312,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           dl[e] = delta[row] * g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
         }
       }
-      if (it >= NSQ && !warp_wait(&s.q_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) break;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int c = lane + 32 * e;
-        s.lse2[st][c] = l2[e];
-        s.delta[st][c] = dl[e];
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&s.q_full[st], 2 * kChunks * Smem::kQChunk);
-        for (int c = 0; c < kChunks; ++c) {
-          tma_load_3d(s.q[st][c], &tm_q, &s.q_full[st], c * 64, q0, b * g.Hq + h);
-          tma_load_3d(s.dout[st][c], &tm_dout, &s.q_full[st], c * 64, q0, b * g.Hq + h);
+      // the group the previous tile freed early first, then the other
+      const int ge = it > 0 ? 1 - (it - 1) / n_it_pass : 0;
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        const int gr = k == 0 ? ge : 1 - ge;
+        if (it > 0 && !warp_wait(&s.grp_empty[gr], (it - 1) & 1, &s.abort_flag, vstatus)) {
+          stopped = true;
+          break;
         }
+        if (k == 0) {  // this tile's row values (slot it & 1: tile it - 2's, read long before)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = lane + 32 * e;
+            s.lse2[it & 1][c] = l2[e];
+            s.delta[it & 1][c] = dl[e];
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&s.grp_full[gr], 2 * kGrp * Smem::kQChunk);
+          for (int c = gr * kGrp; c < (gr + 1) * kGrp; ++c) {
+            tma_load_3d(s.q[0][c], &tm_q, &s.grp_full[gr], c * 64, q0, b * g.Hq + h);
+            tma_load_3d(s.dout[0][c], &tm_dout, &s.grp_full[gr], c * 64, q0, b * g.Hq + h);
+          }
+        }
+        ++issued[gr];
       }
-      ++issued;
     }
     if (lane == 0) {
-      if (issued < n_it) {
+      if (stopped) {
         s.abort_flag = 1;
         atomicOr(status, BD_STATUS_TIMEOUT);
       }
+      // no copy into this CTA's shared memory may still be in flight at exit
       mbar_wait_drain(&s.kv_full, 0);
-      for (int it = (issued > NSQ ? issued - NSQ : 0); it < issued; ++it)
-        mbar_wait_drain(&s.q_full[it % NSQ], (it / NSQ) & 1);
+      for (int gr = 0; gr < 2; ++gr)
+        if (issued[gr] > 0) mbar_wait_drain(&s.grp_full[gr], (issued[gr] - 1) & 1);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
@@ -344,32 +361,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t dMN_k = umma_desc_sw128(0, Smem::kKChunk, 1024);      // MN-major, 128-row chunks
       const uint32_t a_k = smem_u32(s.k[0]), a_v = smem_u32(s.v[0]), a_ds = smem_u32(s.ds);
       const uint32_t a_q = smem_u32(s.q[0][0]), a_do = smem_u32(s.dout[0][0]);
-      constexpr uint32_t kQStage = kChunks * Smem::kQChunk;
-      auto issue_st = [&](uint32_t col, uint32_t a_base, uint32_t b_base) {
+      // X^T = A B^T over the head-dim chunks of group gr (A = K or V, B = Q or dO)
+      auto issue_grp = [&](uint32_t col, uint32_t a_base, uint32_t b_base, int gr, bool first) {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+        for (int kk = 0; kk < 4 * kGrp; ++kk) {
+          const int ks = gr * 4 * kGrp + kk;
           const uint32_t off_a = (ks >> 2) * Smem::kKChunk + (ks & 3) * 32;
           const uint32_t off_b = (ks >> 2) * Smem::kQChunk + (ks & 3) * 32;
           umma_ss(tbase + col, desc_at(dK_major, a_base + off_a), desc_at(dK_major, b_base + off_b), idST,
-                  ks > 0 ? 1u : 0u);
+                  (first && kk == 0) ? 0u : 1u);
         }
       };
       auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
-      bool ok = wait(&s.kv_full, 0) && wait(&s.q_full[0], 0);
-      if (ok) {
+      // S^T and dP^T of tile t: the group the previous tile freed early (and
+      // whose copy started first) first; then the group tile t's dK / dV do not
+      // read is free again once these are done
+      auto issue_sdp = [&](int t) -> bool {
+        const int ge = t > 0 ? 1 - (t - 1) / n_it_pass : 0, gl = 1 - ge;
+        if (!wait(&s.grp_full[ge], t & 1)) return false;
         tc_fence_after();
-        issue_st(Cfg::kColS, a_k, a_q);
+        issue_grp(Cfg::kColS, a_k, a_q, ge, true);
+        issue_grp(Cfg::kColDp, a_v, a_do, ge, true);
+        if (!wait(&s.grp_full[gl], t & 1)) return false;
+        tc_fence_after();
+        issue_grp(Cfg::kColS, a_k, a_q, gl, false);
         umma_commit(&s.s_full);
-        issue_st(Cfg::kColDp, a_v, a_do);
+        issue_grp(Cfg::kColDp, a_v, a_do, gl, false);
         umma_commit(&s.dp_full);
-      }
+        umma_commit(&s.grp_empty[1 - t / n_it_pass]);
+        return true;
+      };
+      bool ok = wait(&s.kv_full, 0) && issue_sdp(0);
       for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % NSQ;
         int pass, h, q0;
         decode(it, pass, h, q0);
         const bool first_of_pass = (it % n_it_pass) == 0;
         const bool last_of_pass = (it % n_it_pass) == n_it_pass - 1;
-        const uint32_t pass_off_q = st * kQStage + pass * (kDp / 64) * Smem::kQChunk;
+        const uint32_t pass_off_q = pass * kGrp * Smem::kQChunk;  // this pass's group of Q / dO chunks
         if (first_of_pass && pass > 0 && !wait(&s.acc_empty, (pass - 1) & 1)) { ok = false; break; }
         // dV += P^T dO[:, pass]; P^T is bf16 in tensor memory, q columns 0-31 at
         // column offset 0 and 32-63 at offset 48 (each half writes over its own S^T)
@@ -380,15 +408,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t a_col = Cfg::kColS + (ks < 2 ? ks * 8 : 48 + (ks - 2) * 8);
           umma_ts(tbase + Cfg::kColDv, tbase + a_col, desc_at(dMN_q, a_do + pass_off_q + ks * 2048), idDKV,
                   (!first_of_pass || ks > 0) ? 1u : 0u);
-        }
-        // S^T of the next q tile goes in now only if its Q has already landed;
-        // otherwise it waits until dK / dQ of this tile have been issued.
-        bool s_next = false;
-        if (NSQ > 1 && it + 1 < n_it && mbar_test_wait(&s.q_full[(it + 1) % NSQ], ((it + 1) / NSQ) & 1)) {
-          tc_fence_after();
-          issue_st(Cfg::kColS, a_k, a_q + ((it + 1) % NSQ) * kQStage);
-          umma_commit(&s.s_full);
-          s_next = true;
         }
         // dK += dS^T Q[:, pass] ; dQ^T = K[:, pass]^T dS^T
         if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
@@ -407,18 +426,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   idDQ, ks > 0 ? 1u : 0u);
         umma_commit(&s.dq_full[bq]);
         umma_commit(&s.ds_empty);
-        umma_commit(&s.q_empty[st]);
+        umma_commit(&s.grp_empty[pass]);  // this pass's group: read by dV, dK above
         if (last_of_pass) umma_commit(&s.acc_full);
-        if (it + 1 < n_it) {
-          const int st1 = (it + 1) % NSQ;
-          if (!s_next) {  // also guarantees dO of the next tile for dP^T below
-            if (!wait(&s.q_full[st1], ((it + 1) / NSQ) & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_st(Cfg::kColS, a_k, a_q + st1 * kQStage);
-            umma_commit(&s.s_full);
-          }
-          issue_st(Cfg::kColDp, a_v, a_do + st1 * kQStage);
-          umma_commit(&s.dp_full);
+        if (it + 1 < n_it && !issue_sdp(it + 1)) {
+          ok = false;
+          break;
         }
       }
       if (!ok) {
@@ -463,10 +475,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int row_end = min(doc_end, win_end);  // rows [key, row_end) attend this key
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int st = it % NSQ;
+      const int st = it & 1;  // slot of this tile's row values
       int pass, h, q0;
       decode(it, pass, h, q0);
-      if (!warp_wait(&s.q_full[st], (it / NSQ) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      // the early group's copy also publishes this tile's row values
+      const int ge = it > 0 ? 1 - (it - 1) / n_it_pass : 0;
+      if (!warp_wait(&s.grp_full[ge], it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       if (!warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[32];
