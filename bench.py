@@ -179,6 +179,26 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+# ------------------------------------------------------- multi-rank bookkeeping
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank's replica draws its own inputs (weak scaling: independent problems)."""
+    return seed + rank
+
+
+def allreduce_max(x: float, device, world: int) -> float:
+    """The slowest rank's time: the job is done when every rank is."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput: the FLOPs every rank did in one step over the step time."""
+    return world * flop_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- our path
 class Replica:
     """Device-resident inputs / outputs of every shard of the workload."""
@@ -490,9 +510,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ranks = None if args.shards is None else {int(x) for x in args.shards.split(",")}
     chunked = args.kv_chunks in ("ring", "ring-merge")
     if chunked:
-        rep = RingChunkReplica(w, args.seed + rank, dev, grad_dtype, ranks, fused=args.kv_chunks == "ring")
+        rep = RingChunkReplica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, fused=args.kv_chunks == "ring")
     else:
-        rep = Replica(w, args.seed + rank, dev, grad_dtype, ranks, deterministic=args.deterministic)
+        rep = Replica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, deterministic=args.deterministic)
     total_flop, fwd_flop, bwd_flop = rep.flops()
 
     def barrier():
@@ -530,10 +550,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     bwd_ms = sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
     merge_ms = sum(a.elapsed_time(b) for e in ev_steps for a, b in e["merge"])
     n_merge = sum(len(e["merge"]) for e in ev_steps)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = allreduce_max(ms, dev, world)
     ms_per_step = ms / args.steps
 
     e2e = None
@@ -543,7 +560,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if rank != 0:
         return None
     peaks = read_peaks()
-    value = world * total_flop / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(total_flop, ms_per_step, world)
     bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     traffic = None
@@ -669,12 +686,8 @@ def run_e2e(rep: Replica, args, total_flop: float, world: int) -> dict:
     torch.cuda.synchronize()
     if int(rep.status.item()) != 0:
         raise RuntimeError(f"device status {int(rep.status.item()):#x} in the end-to-end run")
-    ms = t0.elapsed_time(t1) / steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(world * total_flop / (ms * 1e-3) / 1e12, 2), "unit": UNIT, "ms_per_step": round(ms, 3),
+    ms = allreduce_max(t0.elapsed_time(t1) / steps, dev, world)
+    return {"value": round(job_tflops(total_flop, ms, world), 2), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "copies": "pinned host buffers, overlapped with the kernels on two copy streams"}
 
