@@ -204,10 +204,11 @@ class Replica:
     """Device-resident inputs / outputs of every shard of the workload."""
 
     def __init__(self, w: synth.Workload, seed: int, dev: torch.device, grad_dtype, ranks=None,
-                 deterministic=False):
+                 deterministic=False, fwd_only=False):
         from sliding_window_attention_device_gb300 import bdattn
         self.bd, self.w, self.dev, self.grad_dtype = bdattn, w, dev, grad_dtype
         self.deterministic = deterministic  # dq by the fixed-order pass: bitwise reproducible
+        self.fwd_only = fwd_only  # segments and forward only (head dim 512 has no backward)
         self.doc_np = synth.doc_layout(w.layout, w.B, w.S, seed)
         self.plan = [sh for sh in shard_plan(w, self.doc_np) if ranks is None or sh["r"] in ranks]
         self.doc = torch.from_numpy(self.doc_np).to(dev)
@@ -238,10 +239,14 @@ class Replica:
         self.launches_per_step = (6 if grad_dtype == torch.float32 else 7) * len(self.shards)
         if deterministic:  # delta, zero-fill, dK / dV, dq: one more launch per shard than the fp32 path
             self.launches_per_step = 7 * len(self.shards)
+        if fwd_only:  # segment build, classification, forward
+            self.launches_per_step = 3 * len(self.shards)
 
     def flops(self) -> tuple[float, float, float]:
         D, Hq = self.w.D, self.w.Hq
         pairs = sum(s["pairs"] for s in self.shards)
+        if self.fwd_only:
+            return 4.0 * D * Hq * pairs, 4.0 * D * Hq * pairs, 0.0
         return 14.0 * D * Hq * pairs, 4.0 * D * Hq * pairs, 10.0 * D * Hq * pairs
 
     def run_shard(self, i, ev=None):
@@ -256,6 +261,8 @@ class Replica:
         bd.bd_attn_fwd(s["q"], s["k"], s["v"], s["seg"], g, self.status, out=s["out"], lse=s["lse"])
         if ev is not None:
             ev["fwd"][i][1].record()
+        if self.fwd_only:
+            return
         if self.deterministic:
             if ev is not None:
                 ev["bwd"][i][0].record()
@@ -512,7 +519,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if chunked:
         rep = RingChunkReplica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, fused=args.kv_chunks == "ring")
     else:
-        rep = Replica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, deterministic=args.deterministic)
+        rep = Replica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, deterministic=args.deterministic,
+                      fwd_only=args.fwd_only)
     total_flop, fwd_flop, bwd_flop = rep.flops()
 
     def barrier():
@@ -547,21 +555,22 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         raise RuntimeError(f"device status {int(rep.status.item()):#x} in the timed region")
     ms = start.elapsed_time(stop)
     fwd_ms = sum(e["fwd"][i][0].elapsed_time(e["fwd"][i][1]) for e in ev_steps for i in range(n))
-    bwd_ms = sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
+    fwd_only = getattr(rep, "fwd_only", False)
+    bwd_ms = 0.0 if fwd_only else sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
     merge_ms = sum(a.elapsed_time(b) for e in ev_steps for a, b in e["merge"])
     n_merge = sum(len(e["merge"]) for e in ev_steps)
     ms = allreduce_max(ms, dev, world)
     ms_per_step = ms / args.steps
 
     e2e = None
-    if not args.no_e2e and not chunked:
+    if not args.no_e2e and not chunked and not fwd_only:
         e2e = run_e2e(rep, args, total_flop, world)
 
     if rank != 0:
         return None
     peaks = read_peaks()
     value = job_tflops(total_flop, ms_per_step, world)
-    bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12
+    bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else 0.0
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     traffic = None
     if (TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked
@@ -600,6 +609,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "clocks": clocks,
         "e2e": e2e,
     }
+    if fwd_only:
+        fwd_s = fwd_ms * 1e-3 / (args.steps * len(rep.shards))
+        fwd_achieved = fwd_flop / len(rep.shards) / fwd_s / 1e12
+        line["metric"] = "fwd TFLOP/s (unmasked FLOPs) and % of GB300 dense BF16 peak, 1 GPU"
+        line["e2e_note"] = "forward only: the end-to-end timing covers the whole path"
+        line["roofline"] = {"kernel": f"fwd{'512' if w.D == 512 else ''}_kernel (forward, D {w.D})", "bound": "tensor",
+                            "achieved": round(fwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                            "frac": round(fwd_achieved / peak, 4),
+                            "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
+                            "traffic": None, "flops_per_launch": fwd_flop / len(rep.shards),
+                            "avg_launch_ms": round(fwd_s * 1e3, 4)}
+        del line["bwd_main_tflops"]
     if chunked:
         line["e2e_note"] = "end-to-end timing is taken on the unchunked path only"
         if n_merge:
@@ -775,6 +796,8 @@ def main():
     ap.add_argument("--grad-dtype", choices=("f32", "bf16"), default="f32")
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="segments and forward only (the head-dim-512 workload G512 has no backward)")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise reproducible backward (dq by a fixed-order pass instead of atomic additions)")
     ap.add_argument("--exchange", action="store_true",

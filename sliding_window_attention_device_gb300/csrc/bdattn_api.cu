@@ -16,6 +16,8 @@ cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, in
                              int kv_chunk);
 cudaError_t launch_merge(const Geom& g, void* out, float* lse, const void* out_c, const float* lse_c,
                          const int32_t* status, cudaStream_t st);
+cudaError_t launch_fwd512(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
+                          const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st);
 cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
@@ -91,7 +93,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int to_geom(const bd_geom* in, Geom* g) {
   if (!in) return BD_ERR_ARG;
   if (in->B < 1 || in->Hq < 1 || in->Hkv < 1 || in->Hq % in->Hkv != 0) return BD_ERR_ARG;
-  if (in->D != 64 && in->D != 128 && in->D != 256) return BD_ERR_ARG;
+  if (in->D != 64 && in->D != 128 && in->D != 256 && in->D != 512) return BD_ERR_ARG;
   if (in->L < 1 || in->S_kv < 1 || in->S_full < 1) return BD_ERR_ARG;
   if (in->row_offset < 0 || static_cast<long long>(in->row_offset) + in->L > in->S_full) return BD_ERR_ARG;
   if (in->kv_offset < 0 || static_cast<long long>(in->kv_offset) + in->S_kv > in->S_full) return BD_ERR_ARG;
@@ -231,6 +233,7 @@ int bd_attn_merge(void* out, float* lse, const void* out_chunk, const float* lse
   if (int rc = to_geom(gi, &g)) return rc;
   if (!out || !lse || !out_chunk || !lse_chunk || !status) return BD_ERR_ARG;
   if (!aligned16(out) || !aligned16(out_chunk)) return BD_ERR_ARG;
+  if (g.D == 512) return BD_ERR_ARG;  // the merge kernel takes D <= 256
   if (int rc = check_device()) return rc;
   return cuda_rc(launch_merge(g, out, lse, out_chunk, lse_chunk, status, static_cast<cudaStream_t>(stream)));
 }
@@ -290,10 +293,14 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* seg, const
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(seg)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
+  if (g.D == 512 && merge) return BD_ERR_ARG;  // the merging epilogue takes D <= 256
   CUtensorMap mq, mk, mv;
   if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map_kv(&mk, k, g, kTile) ||
       make_map_kv(&mv, v, g, kTile))
     return BD_ERR_CUDA;
+  if (g.D == 512)
+    return cuda_rc(launch_fwd512(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status,
+                                 static_cast<cudaStream_t>(stream)));
   return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status, merge,
                             static_cast<cudaStream_t>(stream)));
 }
@@ -318,6 +325,7 @@ int bwd_prep_impl(const void* dout, const void* out, const bd_geom* gi, void* wo
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dout || !out || !workspace || !status) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
   if (dq_f32 && !aligned16(dq_f32)) return BD_ERR_ARG;
@@ -330,6 +338,7 @@ int bwd_main_impl(const void* dout, const void* q, const void* k, const void* v,
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dout || !q || !k || !v || !lse || !seg || !dk || !dv || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) ||
@@ -380,6 +389,7 @@ int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* work
                          bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dq || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dq) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
@@ -420,6 +430,7 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
                 int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   // check everything up front so that a bad argument enqueues nothing
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
@@ -476,6 +487,7 @@ int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const vo
                         void* dv, int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
+  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (bwd_workspace_bytes(g) > BD_NOALLOC_SCRATCH_BYTES) return BD_ERR_SCRATCH_TOO_SMALL;
   if (int rc = check_device()) return rc;
   void* scratch = nullptr;

@@ -1,0 +1,81 @@
+"""Head dim 512 (the Gemma4 global layers: gemma4_moe.cp_attention, D = 512
+full-attention layers) through bd_attn_fwd on the GPU -- the split-D forward
+(Q resident, K streamed in 64-column chunks, O in two 256-column passes) --
+against the oracle: several q tiles with a ragged tail, GQA, a window,
+token-major K/V, and sampled rows of the full-size workload. The backward
+entry points refuse D = 512."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import LSE_ABS, assert_close, make_case, oracle_geom, real_rows
+from sliding_window_attention_device_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+W_ = synth.Workload
+CASES = [
+    ("g2_ragged", W_("ga", "D 512, GQA 2, ragged", B=2, Hq=4, Hkv=2, D=512, S=1280, cp_size=4,
+                     layout=("uniform", 20, 500, 40)), 2, 0),
+    ("g1_window", W_("gb", "D 512, window 200", B=1, Hq=2, Hkv=2, D=512, S=1024, cp_size=2,
+                     layout=("uniform", 100, 900, 30), window=200), 1, 0),
+    ("g4_token_major", W_("gc", "D 512, GQA 4, token-major", B=1, Hq=4, Hkv=1, D=512, S=768, cp_size=3,
+                          layout=("uniform", 64, 700, 10), kv="prefix"), 2, 1),
+]
+
+
+def _fwd(c, layout):
+    from sliding_window_attention_device_gb300 import bdattn
+    w, dev = c["w"], torch.device("cuda")
+    g = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], w.window,
+                    kv_layout=layout)
+    to = (lambda t: t.permute(2, 0, 1, 3).contiguous()) if layout else (lambda t: t)
+    doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
+    q, k, v = c["q"].to(dev), to(c["k"]).to(dev), to(c["v"]).to(dev)
+    seg, status = bdattn.bd_attn_seg_build(doc, g)
+    out = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((w.B, w.Hq, w.L), float("nan"), dtype=torch.float32, device=dev)
+    bdattn.bd_attn_fwd(q, k, v, seg, g, status, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return g, seg, status, out, lse, (q, k, v, doc)
+
+
+@pytest.mark.parametrize("name,w,r,layout", CASES, ids=[x[0] for x in CASES])
+def test_d512_forward(name, w, r, layout):
+    c = make_case(w, r)
+    _, _, _, out, lse, _ = _fwd(c, layout)
+    ref_out, ref_lse = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], oracle_geom(c))
+    assert_close(f"{name} out", out, ref_out)
+    real = real_rows(c)
+    got = lse.double().cpu().numpy()
+    assert np.isneginf(got[~real]).all()
+    assert np.abs(got[real] - ref_lse[real]).max(initial=0.0) <= LSE_ABS
+
+
+def test_d512_backward_refused():
+    from sliding_window_attention_device_gb300 import bdattn
+    c = make_case(CASES[0][1], CASES[0][2])
+    g, seg, status, out, lse, (q, k, v, _) = _fwd(c, 0)
+    with pytest.raises(RuntimeError):
+        bdattn.bd_attn_bwd(c["do"].cuda(), q, k, v, out, lse, seg, g, status)
+    with pytest.raises(RuntimeError):
+        bdattn.bd_attn_fwd_merge(q, k, v, seg, g, status, out, lse)
+
+
+@pytest.mark.slow
+def test_d512_full_size_sampled():
+    w = synth.WORKLOADS["G512"]
+    rng = np.random.default_rng(5)
+    for r in (3, 7):
+        c = make_case(w, r, seed=0)
+        _, _, _, out, lse, _ = _fwd(c, 0)
+        out, lse = out.float().cpu(), lse.cpu()
+        rows = sorted({(0, int(rng.integers(w.Hq)), int(i)) for i in rng.integers(0, w.L, 40)})
+        ref_out, ref_lse = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], oracle_geom(c), rows=rows)
+        for t, (b, h, i) in enumerate(rows):
+            d = np.abs(out[b, h, i].numpy() - ref_out[t])
+            assert d.max() <= 2e-2, (r, b, h, i, d.max())
+            if np.isfinite(ref_lse[t]):
+                assert abs(float(lse[b, h, i]) - ref_lse[t]) <= LSE_ABS
