@@ -9,7 +9,10 @@
 //           and written with lse at the end of the pass;
 //   pass 1: S recomputed, P = 2^(scale log2(e) s - lse log2(e)) -- already
 //           normalised, no running max -- and O[:, 256:512] += P V[:, 256:512].
-//   warp 0   TMA: Q once, K chunks through a 2-slot ring, a V half per tile
+// S is double-buffered (step t in buffer t & 1), so the next step's S = Q K^T
+// runs while the softmax works on this one.
+//   warp 0   TMA: Q once, K chunks through a 2-slot ring (K one step ahead of V),
+//            a V half per tile
 //   warp 1   one thread issues the MMAs      warp 2  tensor memory
 //   warps 4-7  thread = q row: softmax, P (bf16 over S in tensor memory), out
 #include <cuda.h>
@@ -27,7 +30,7 @@ constexpr int kQChunks = kD512 / 64;        // 8 chunks of 64 columns
 constexpr int kChunkB = kTile * 128;        // 128 rows x 128 B
 constexpr int kKSlots = 2;                  // K chunk ring
 constexpr int kVChunks = 4;                 // one 256-column half of V
-constexpr uint32_t kColS = 0, kColO = 128;  // S / P: 128 columns; O half: 256 columns
+constexpr uint32_t kColS = 0, kColO = 256;  // S / P: two 128-column buffers; O half: 256 columns
 constexpr int kThreads512 = 256;
 
 struct Fwd512Smem {
@@ -35,7 +38,10 @@ struct Fwd512Smem {
   alignas(1024) uint8_t k[kKSlots][kChunkB];
   alignas(1024) uint8_t v[kVChunks][kChunkB];
   uint64_t q_full, k_full[kKSlots], k_empty[kKSlots], v_full, v_empty;
-  uint64_t s_full, p_full, o_done, o_free, mma_drain;
+  // per S buffer, so that each has at most one phase outstanding when waited
+  // on: step t's S completes only after step t - 2's PV product
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t o_free, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
   int b, qt, kt_lo, nk, n_real, skip;
@@ -82,9 +88,11 @@ __global__ void __launch_bounds__(kThreads512, 1)
     }
     mbar_init(&s.v_full, 1);
     mbar_init(&s.v_empty, 1);
-    mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 128);
+      mbar_init(&s.o_done[i], 1);
+    }
     mbar_init(&s.o_free, 128);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
@@ -123,30 +131,37 @@ __global__ void __launch_bounds__(kThreads512, 1)
     mbar_arrive_expect_tx(&s.q_full, kQChunks * kChunkB);
     for (int c = 0; c < kQChunks; ++c) tma_load_3d(s.q[c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h);
     const int pl = b * g.Hkv + hk;
-    int kc = 0, vt = 0;  // K chunks and V halves issued
+    const int total = 2 * nk;  // (pass, tile) steps
+    int kc = 0, vt = 0;        // K chunks and V halves issued
     bool stop = false;
-    for (int p = 0; p < 2 && !stop; ++p) {
-      for (int j = 0; j < nk && !stop; ++j) {
-        const int row = (kt_lo + j) * kTile;
-        for (int c = 0; c < kQChunks; ++c, ++kc) {
-          const int slot = kc % kKSlots;
-          if (kc >= kKSlots && !pipe_wait(&s.k_empty[slot], (kc / kKSlots - 1) & 1, &s.abort_flag, vstatus)) {
-            stop = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&s.k_full[slot], kChunkB);
-          tma_load_3d(s.k[slot], &tm_k, &s.k_full[slot], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
-        }
-        if (stop) break;
-        if (vt > 0 && !pipe_wait(&s.v_empty, (vt - 1) & 1, &s.abort_flag, vstatus)) {
-          stop = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&s.v_full, kVChunks * kChunkB);
-        for (int c = 0; c < kVChunks; ++c)
-          tma_load_3d(s.v[c], &tm_v, &s.v_full, (kVChunks * p + c) * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
-        ++vt;
+    // K of step u (8 chunks through the ring)
+    auto load_k = [&](int u) {
+      const int row = (kt_lo + u % nk) * kTile;
+      for (int c = 0; c < kQChunks; ++c, ++kc) {
+        const int slot = kc % kKSlots;
+        if (kc >= kKSlots && !pipe_wait(&s.k_empty[slot], (kc / kKSlots - 1) & 1, &s.abort_flag, vstatus))
+          return false;
+        mbar_arrive_expect_tx(&s.k_full[slot], kChunkB);
+        tma_load_3d(s.k[slot], &tm_k, &s.k_full[slot], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
       }
+      return true;
+    };
+    // K runs one step ahead of V, in the order the MMAs use them: S(0), S(1),
+    // PV(0), S(2), PV(1), ...
+    for (int t = 0; t < total && !stop; ++t) {
+      if ((t == 0 && !load_k(0)) || (t + 1 < total && !load_k(t + 1))) {
+        stop = true;
+        break;
+      }
+      if (vt > 0 && !pipe_wait(&s.v_empty, (vt - 1) & 1, &s.abort_flag, vstatus)) {
+        stop = true;
+        break;
+      }
+      const int row = (kt_lo + t % nk) * kTile, p = t / nk;
+      mbar_arrive_expect_tx(&s.v_full, kVChunks * kChunkB);
+      for (int c = 0; c < kVChunks; ++c)
+        tma_load_3d(s.v[c], &tm_v, &s.v_full, (kVChunks * p + c) * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
+      ++vt;
     }
     if (stop) {
       s.abort_flag = 1;
@@ -164,39 +179,44 @@ __global__ void __launch_bounds__(kThreads512, 1)
     const uint64_t dMN = umma_desc_sw128(0, kChunkB, 1024);          // 16 KB between 64-column chunks
     const uint32_t a_q = smem_u32(s.q[0]), a_k = smem_u32(s.k[0]), a_v = smem_u32(s.v[0]);
     auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
-    bool ok = wait(&s.q_full, 0);
-    int kc = 0, t = 0;  // K chunks consumed, (pass, tile) steps
-    for (int p = 0; ok && p < 2; ++p) {
-      for (int j = 0; ok && j < nk; ++j, ++t) {
-        // S = Q K^T over the 8 head-dim chunks (this step's PV product was issued
-        // after the previous one's, so P is read before S is overwritten)
-        for (int c = 0; c < kQChunks; ++c, ++kc) {
-          const int slot = kc % kKSlots;
-          if (!wait(&s.k_full[slot], (kc / kKSlots) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_ss(tbase + kColS, desc_at(dK_major, a_q + c * kChunkB + ks * 32),
-                    desc_at(dK_major, a_k + slot * kChunkB + ks * 32), idS, (c > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&s.k_empty[slot]);
-        }
-        if (!ok) break;
-        umma_commit(&s.s_full);
-        // O half += P V half (pass 1 starts once pass 0's O has been read out)
-        if (!wait(&s.p_full, t & 1) || !wait(&s.v_full, t & 1) || (p == 1 && j == 0 && !wait(&s.o_free, 0))) {
-          ok = false;
-          break;
-        }
+    const int total = 2 * nk;  // (pass, tile) steps
+    int kc = 0;                // K chunks consumed
+    // S(u) = Q K^T over the 8 head-dim chunks into buffer u & 1
+    auto issue_s = [&](int u) {
+      const uint32_t d = tbase + kColS + (u & 1) * 128;
+      for (int c = 0; c < kQChunks; ++c, ++kc) {
+        const int slot = kc % kKSlots;
+        if (!wait(&s.k_full[slot], (kc / kKSlots) & 1)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ts(tbase + kColO, tbase + kColS + ks * 8, desc_at(dMN, a_v + ks * 2048), idPV,
-                  (j > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(&s.v_empty);
-        umma_commit(&s.o_done);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_ss(d, desc_at(dK_major, a_q + c * kChunkB + ks * 32), desc_at(dK_major, a_k + slot * kChunkB + ks * 32),
+                  idS, (c > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&s.k_empty[slot]);
+      }
+      umma_commit(&s.s_full[u & 1]);
+      return true;
+    };
+    bool ok = wait(&s.q_full, 0) && issue_s(0) && (total < 2 || issue_s(1));
+    for (int t = 0; ok && t < total; ++t) {
+      const int p = t / nk, j = t - p * nk;
+      // O half += P V half (pass 1 starts once pass 0's O has been read out)
+      if (!wait(&s.p_full[t & 1], (t >> 1) & 1) || !wait(&s.v_full, t & 1) ||
+          (p == 1 && j == 0 && !wait(&s.o_free, 0))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kTile / 16; ++ks)
+        umma_ts(tbase + kColO, tbase + kColS + (t & 1) * 128 + ks * 8, desc_at(dMN, a_v + ks * 2048), idPV,
+                (j > 0 || ks > 0) ? 1u : 0u);
+      umma_commit(&s.v_empty);
+      umma_commit(&s.o_done[t & 1]);
+      // S two steps on goes into the buffer this PV product reads (issued after it)
+      if (t + 2 < total && !issue_s(t + 2)) {
+        ok = false;
+        break;
       }
     }
     if (!ok) {
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(kThreads512, 1)
     // ------------------------------------------------ softmax (thread = row)
     const int r = tid - 128;  // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tbase + lane_off + kColS, t_o = tbase + lane_off + kColO;
+    const uint32_t t_o = tbase + lane_off + kColO;
     const int i = qt * kTile + r;
     const bool real = i < n_real;
     int jlo = 1, jhi = 0;  // allowed K/V buffer rows [jlo, jhi] of this row
@@ -226,11 +246,12 @@ __global__ void __launch_bounds__(kThreads512, 1)
     int t = 0;
     for (int p = 0; p < 2 && ok; ++p) {
       for (int j = 0; j < nk; ++j, ++t) {
-        if (!warp_wait(&s.s_full, t & 1, &s.abort_flag, vstatus)) {
+        if (!warp_wait(&s.s_full[t & 1], (t >> 1) & 1, &s.abort_flag, vstatus)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t t_s = tbase + lane_off + kColS + (t & 1) * 128;  // this step's S buffer
         uint32_t xr[128];
         tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
         tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
@@ -260,7 +281,7 @@ __global__ void __launch_bounds__(kThreads512, 1)
               m = m_new;
             }
             if (j > 0) {  // rescale the running O once its last product is done
-              if (!warp_wait(&s.o_done, (t - 1) & 1, &s.abort_flag, vstatus)) {
+              if (!warp_wait(&s.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &s.abort_flag, vstatus)) {
                 ok = false;
                 break;
               }
@@ -309,11 +330,12 @@ __global__ void __launch_bounds__(kThreads512, 1)
         tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&s.p_full);
+        mbar_arrive(&s.p_full[t & 1]);
       }
       ok = __all_sync(0xffffffffu, ok);
       // end of the pass: this half of O, once its last product is done
-      if (ok && !warp_wait(&s.o_done, (t - 1) & 1, &s.abort_flag, vstatus)) ok = false;
+      // (PV products complete in order: the last one's completion covers the rest)
+      if (ok && !warp_wait(&s.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &s.abort_flag, vstatus)) ok = false;
       if (!ok) break;
       tc_fence_after();
       float scale_o = 1.0f;
