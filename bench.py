@@ -54,7 +54,10 @@ UNIT = "TFLOP/s"
 # kernel, the mean over the 8 launches (one per shard) of one bench step, from
 # `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` (see profiles/);
 # valid only for the kernel sources whose hash is recorded here.
-TRAFFIC = {"kernel": "bwd128_kernel<128>", "source_sha256": "cd9d083444a3a85a", "bytes_per_launch": 1.16909e9}
+# the backward main-stage kernel of each head dim
+BWD_KERNEL = {64: "bwd128_kernel<64>", 128: "bwd128_kernel<128>", 256: "bwd_kernel<256>",
+              512: "bwd512_kernel (four CTAs per K/V tile, one per 128-column slice)"}
+TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "cd9d083444a3a85a", "bytes_per_launch": 1.16909e9}
 
 
 # ------------------------------------------------------------------ workload
@@ -208,7 +211,7 @@ class Replica:
         from sliding_window_attention_device_gb300 import bdattn
         self.bd, self.w, self.dev, self.grad_dtype = bdattn, w, dev, grad_dtype
         self.deterministic = deterministic  # dq by the fixed-order pass: bitwise reproducible
-        self.fwd_only = fwd_only  # segments and forward only (head dim 512 has no backward)
+        self.fwd_only = fwd_only  # segments and forward only
         self.doc_np = synth.doc_layout(w.layout, w.B, w.S, seed)
         self.plan = [sh for sh in shard_plan(w, self.doc_np) if ranks is None or sh["r"] in ranks]
         self.doc = torch.from_numpy(self.doc_np).to(dev)
@@ -574,7 +577,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     traffic = None
     if (TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked
-            and not getattr(rep, "deterministic", False)):
+            and w.key == TRAFFIC["workload"] and not getattr(rep, "deterministic", False)):
         traffic = TRAFFIC["bytes_per_launch"]  # measured per whole-shard launch, not per chunk
     n_bwd = sum(len(s["chunks"]) for s in rep.shards) if chunked else len(rep.shards)
     fwd_kernel_ms = fwd_ms - merge_ms  # the forward region less its merges
@@ -596,9 +599,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
-        "roofline": {"kernel": ("backward: delta, zero-fill, bwd128_kernel<128> without dq, bwd_dq_kernel<128>"
+        "roofline": {"kernel": (f"backward: delta, zero-fill, bwd128_kernel<{w.D}> without dq, bwd_dq_kernel<{w.D}>"
                                 if getattr(rep, "deterministic", False) else
-                                "bwd128_kernel<128> (backward main stage, with its dK/dV zero-fill launch)"),
+                                f"{BWD_KERNEL[w.D]} (backward main stage, with its dK/dV zero-fill launch)"),
                      "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
                      "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
@@ -797,7 +800,7 @@ def main():
     ap.add_argument("--shards", default=None, help="comma-separated cp ranks to run (default: all of the workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
-                    help="segments and forward only (the head-dim-512 workload G512 has no backward)")
+                    help="segments and forward only")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise reproducible backward (dq by a fixed-order pass instead of atomic additions)")
     ap.add_argument("--exchange", action="store_true",
@@ -806,8 +809,9 @@ def main():
                     help="ring: each shard's K/V in per-rank chunks, each chunk's forward merged in its epilogue, "
                          "backward per chunk; ring-merge: the same with the separate merge kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-heads", type=int, default=32,
-                    help="query heads of batch row 0 in the oracle's timed CPU-baseline slice")
+    ap.add_argument("--cpu-heads", type=int, default=None,
+                    help="query heads of batch row 0 in the oracle's timed CPU-baseline slice "
+                         "(default: about 10-30 s of CPU work; 8 for head dim 512, else 32)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -836,7 +840,9 @@ def main():
         line = run_ours(args, rank, world, local_rank)
         if line is not None:
             if world == 1 and not args.no_cpu_baseline:
-                line["cpu_baseline"] = cpu_baseline(synth.WORKLOADS[args.config], args.seed, args.cpu_heads)
+                wk = synth.WORKLOADS[args.config]
+                heads = args.cpu_heads if args.cpu_heads is not None else (8 if wk.D >= 512 else 32)
+                line["cpu_baseline"] = cpu_baseline(wk, args.seed, heads)
             print(json.dumps(line), flush=True)
     finally:
         if world > 1:

@@ -32,9 +32,9 @@
  *   lse      fp32  [B, Hq,  L]        natural-log sum-exp; -inf on padding rows
  *   dq       fp32 or bf16 [B, Hq, L, D]
  *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group (k's layout)
- * D must be 64, 128 or 256, or 512 for the forward alone (bd_attn_fwd; the
- * backward entry points, the merge and the merging forward return BD_ERR_ARG
- * for it). All device pointers are caller-owned and must be
+ * D must be 64, 128, 256 or 512 (the head-dim-512 global layers of
+ * gemma4_moe.cp_attention; for D = 512 the merge, the merging forward and the
+ * fixed-order backward return BD_ERR_ARG). All device pointers are caller-owned and must be
  * 16-byte aligned. The library allocates no device memory and never
  * synchronises the stream; every entry point only enqueues work on `stream`.
  *
@@ -62,7 +62,7 @@ typedef struct {
   int B;          /* batch rows */
   int Hq;         /* query heads */
   int Hkv;        /* key/value heads; Hq % Hkv == 0 */
-  int D;          /* head dim: 64, 128 or 256; 512 for the forward only */
+  int D;          /* head dim: 64, 128, 256 or 512 */
   int S_full;     /* length of each doc_ids row (full padded sequence) */
   int L;          /* local query rows */
   int row_offset; /* global position of local row 0 */

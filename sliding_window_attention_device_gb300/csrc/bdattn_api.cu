@@ -325,7 +325,6 @@ int bwd_prep_impl(const void* dout, const void* out, const bd_geom* gi, void* wo
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dout || !out || !workspace || !status) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
   if (dq_f32 && !aligned16(dq_f32)) return BD_ERR_ARG;
@@ -338,7 +337,6 @@ int bwd_main_impl(const void* dout, const void* q, const void* k, const void* v,
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dout || !q || !k || !v || !lse || !seg || !dk || !dv || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) ||
@@ -389,7 +387,6 @@ int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* work
                          bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (!dq || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dq) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
@@ -430,7 +427,6 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
                 int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   // check everything up front so that a bad argument enqueues nothing
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
@@ -487,7 +483,6 @@ int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const vo
                         void* dv, int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D == 512) return BD_ERR_ARG;  // no backward for D = 512
   if (bwd_workspace_bytes(g) > BD_NOALLOC_SCRATCH_BYTES) return BD_ERR_SCRATCH_TOO_SMALL;
   if (int rc = check_device()) return rc;
   void* scratch = nullptr;

@@ -49,30 +49,37 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       long long n_rows, const int32_t* status) {
   pdl_begin();
   if (*reinterpret_cast<const volatile int*>(status) != 0) return;
-  constexpr int kLanes = D / 8;  // threads per row, 8 elements (16 B) each
+  constexpr int kLanes = D / 8 < 32 ? D / 8 : 32;  // threads per row
+  constexpr int kVec = D / 8 / kLanes;              // 8-element (16 B) pieces per thread
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_rows * kLanes;
        t += nthreads) {
     const long long row = t / kLanes;
     const int part = static_cast<int>(t % kLanes);
-    const uint4 a = reinterpret_cast<const uint4*>(dout + row * D)[part];
-    const uint4 o = reinterpret_cast<const uint4*>(out + row * D)[part];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
     float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(o2[e]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+    for (int u = 0; u < kVec; ++u) {
+      const uint4 a = reinterpret_cast<const uint4*>(dout + row * D)[part + u * kLanes];
+      const uint4 o = reinterpret_cast<const uint4*>(out + row * D)[part + u * kLanes];
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(o2[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
     }
 #pragma unroll
     for (int o = kLanes / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o, kLanes);
     if (part == 0) delta[row] = acc;
     if (dq_acc) {  // none: delta only (the fixed-order dq pass writes dq itself)
-      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + row * D + (part + u * kLanes) * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -729,13 +736,15 @@ cudaError_t launch_pre(const Geom& g, const void* dout, const void* out, void* w
   const __nv_bfloat16* dob = static_cast<const __nv_bfloat16*>(dout);
   const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(out);
   float* delta = ws_delta(g, workspace);
-  const unsigned grid = grid_for(rows * (g.D / 8));
+  const unsigned grid = grid_for(rows * (g.D / 8 < 32 ? g.D / 8 : 32));
   switch (g.D) {
     case 64: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<64>, dim3(grid), dim3(256), 0, st, dob, ob, delta,
         dq_acc, rows, status); le != cudaSuccess) return le; break;
     case 128: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<128>, dim3(grid), dim3(256), 0, st, dob, ob,
         delta, dq_acc, rows, status); le != cudaSuccess) return le; break;
     case 256: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<256>, dim3(grid), dim3(256), 0, st, dob, ob,
+        delta, dq_acc, rows, status); le != cudaSuccess) return le; break;
+    case 512: if (const cudaError_t le = launch_pdl(bwd_pre_kernel<512>, dim3(grid), dim3(256), 0, st, dob, ob,
         delta, dq_acc, rows, status); le != cudaSuccess) return le; break;
     default: return cudaErrorInvalidValue;
   }
@@ -744,6 +753,10 @@ cudaError_t launch_pre(const Geom& g, const void* dout, const void* out, void* w
 }  // namespace
 
 cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                               const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
+                               cudaStream_t st);
+cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
                                cudaStream_t st);
@@ -774,6 +787,8 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
       return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 256:
       return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 512:  // the head dim of the outputs split over four CTAs (bwd512_kernel.cu)
+      return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
 }

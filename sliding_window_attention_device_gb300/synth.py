@@ -76,7 +76,7 @@ WORKLOADS = {
     "C5w4096": Workload("C5w4096", "many short docs, needed-range K/V, window 4096", B=4, Hq=32, Hkv=4, D=128,
                         S=65536, cp_size=8, layout=("uniform", 128, 4096, 0), window=4096,
                         ranks=tuple(range(8)), kv="needed"),
-    "G512": Workload("G512", "Gemma4-style global layer, head dim 512 (forward)", B=1, Hq=16, Hkv=4, D=512,
+    "G512": Workload("G512", "Gemma4-style global layer, head dim 512", B=1, Hq=16, Hkv=4, D=512,
                      S=32768, cp_size=8, layout=("uniform", 512, 16384, 511), window=0, ranks=tuple(range(8)),
                      kv="prefix"),
     "C5w512": Workload("C5w512", "many short docs, needed-range K/V, window 512", B=4, Hq=32, Hkv=4, D=128,

@@ -1,9 +1,15 @@
 """Head dim 512 (the Gemma4 global layers: gemma4_moe.cp_attention, D = 512
-full-attention layers) through bd_attn_fwd on the GPU -- the split-D forward
-(Q resident, K streamed in 64-column chunks, O in two 256-column passes) --
-against the oracle: several q tiles with a ragged tail, GQA, a window,
-token-major K/V, and sampled rows of the full-size workload. The backward
-entry points refuse D = 512."""
+full-attention layers, `_ffpa_varlen_forward_chunk` / `_ffpa_varlen_backward_chunk`)
+on the GPU against the oracle:
+
+  * the split-D forward (Q resident, K streamed in 64-column chunks, O in two
+    256-column passes) through bd_attn_fwd;
+  * the backward through bd_attn_bwd (dK / dV / dQ columns split over four
+    CTAs per K/V tile, S and dP formed in each): fp32 and bf16 gradients;
+  * several q tiles with a ragged tail, GQA, a window, token-major K/V, and
+    sampled rows / keys of the full-size workload.
+The entry points without a D = 512 path (the merging epilogue, the fixed-order
+backward) refuse it."""
 import numpy as np
 import pytest
 import torch
@@ -54,14 +60,50 @@ def test_d512_forward(name, w, r, layout):
     assert np.abs(got[real] - ref_lse[real]).max(initial=0.0) <= LSE_ABS
 
 
-def test_d512_backward_refused():
+def _bwd(c, g, seg, status, out, lse, qkv, layout, grad_dtype=torch.float32):
+    from sliding_window_attention_device_gb300 import bdattn
+    q, k, v, _ = qkv
+    w, dev = c["w"], q.device
+    dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=grad_dtype, device=dev)
+    dk = torch.full(bdattn.kv_shape(g), float("nan"), dtype=grad_dtype, device=dev)
+    dv = torch.full_like(dk, float("nan"))
+    bdattn.bd_attn_bwd(c["do"].to(dev), q, k, v, out, lse, seg, g, status, grad_dtype=grad_dtype, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    back = (lambda t: t.permute(1, 2, 0, 3)) if layout else (lambda t: t)
+    return dq.cpu(), back(dk).cpu(), back(dv).cpu()
+
+
+@pytest.mark.parametrize("name,w,r,layout", CASES, ids=[x[0] for x in CASES])
+def test_d512_backward(name, w, r, layout):
+    c = make_case(w, r)
+    g, seg, status, out, lse, qkv = _fwd(c, layout)
+    dq, dk, dv = _bwd(c, g, seg, status, out, lse, qkv, layout)
+    rdq, rdk, rdv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], oracle_geom(c))
+    assert_close(f"{name} dq", dq, rdq)
+    assert_close(f"{name} dk", dk, rdk)
+    assert_close(f"{name} dv", dv, rdv)
+
+
+def test_d512_backward_bf16_gradients():
+    c = make_case(CASES[0][1], CASES[0][2])
+    g, seg, status, out, lse, qkv = _fwd(c, 0)
+    f = _bwd(c, g, seg, status, out, lse, qkv, 0)
+    h = _bwd(c, g, seg, status, out, lse, qkv, 0, torch.bfloat16)
+    for a, b_, n in zip(h, f, ("dq", "dk", "dv")):
+        assert torch.isfinite(a.float()).all(), n
+        tol = 2.0 ** -7 * max(1.0, b_.abs().max().item())
+        assert (a.float() - b_).abs().max().item() <= tol, n
+
+
+def test_d512_refused_where_unbuilt():
     from sliding_window_attention_device_gb300 import bdattn
     c = make_case(CASES[0][1], CASES[0][2])
     g, seg, status, out, lse, (q, k, v, _) = _fwd(c, 0)
     with pytest.raises(RuntimeError):
-        bdattn.bd_attn_bwd(c["do"].cuda(), q, k, v, out, lse, seg, g, status)
-    with pytest.raises(RuntimeError):
         bdattn.bd_attn_fwd_merge(q, k, v, seg, g, status, out, lse)
+    with pytest.raises(RuntimeError):
+        bdattn.bd_attn_bwd_deterministic(c["do"].cuda(), q, k, v, out, lse, seg, g, status)
 
 
 @pytest.mark.slow
@@ -79,3 +121,20 @@ def test_d512_full_size_sampled():
             assert d.max() <= 2e-2, (r, b, h, i, d.max())
             if np.isfinite(ref_lse[t]):
                 assert abs(float(lse[b, h, i]) - ref_lse[t]) <= LSE_ABS
+
+
+@pytest.mark.slow
+def test_d512_backward_full_size_sampled():
+    from test_gpu_full import _check, _oracle_sampled, _pick
+    w = synth.WORKLOADS["G512"]
+    r = 5
+    c = make_case(w, r, seed=0)
+    g, seg, status, out, lse, qkv = _fwd(c, 0)
+    dq, dk, dv = _bwd(c, g, seg, status, out, lse, qkv, 0)
+    rows, keys = _pick(c, np.random.default_rng(31))
+    ref_rows, ref_keys = _oracle_sampled(c, rows, keys)
+    for (bb, h, i), (_, _, dq_ref) in ref_rows.items():
+        _check(f"G512 r{r} dq[{bb},{h},{i}]", dq[bb, h, i].numpy(), dq_ref)
+    for (bb, hk, j), (dk_ref, dv_ref) in ref_keys.items():
+        _check(f"G512 r{r} dk[{bb},{hk},{j}]", dk[bb, hk, j].numpy(), dk_ref)
+        _check(f"G512 r{r} dv[{bb},{hk},{j}]", dv[bb, hk, j].numpy(), dv_ref)
