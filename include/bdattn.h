@@ -33,8 +33,8 @@
  *   dq       fp32 or bf16 [B, Hq, L, D]
  *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group (k's layout)
  * D must be 64, 128, 256 or 512 (the head-dim-512 global layers of
- * gemma4_moe.cp_attention; for D = 512 the merge, the merging forward and the
- * fixed-order backward return BD_ERR_ARG). All device pointers are caller-owned and must be
+ * gemma4_moe.cp_attention; for D = 512 the fixed-order backward returns
+ * BD_ERR_ARG). All device pointers are caller-owned and must be
  * 16-byte aligned. The library allocates no device memory and never
  * synchronises the stream; every entry point only enqueues work on `stream`.
  *

@@ -17,7 +17,7 @@ cudaError_t launch_seg_build(const int32_t* doc, const Geom& g, int32_t* seg, in
 cudaError_t launch_merge(const Geom& g, void* out, float* lse, const void* out_c, const float* lse_c,
                          const int32_t* status, cudaStream_t st);
 cudaError_t launch_fwd512(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
-                          const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st);
+                          const Geom& g, void* out, float* lse, int32_t* status, bool merge, cudaStream_t st);
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st);
 cudaError_t launch_bwd_prep(const Geom& g, const void* dout, const void* out, void* workspace, float* dq_f32,
@@ -233,7 +233,6 @@ int bd_attn_merge(void* out, float* lse, const void* out_chunk, const float* lse
   if (int rc = to_geom(gi, &g)) return rc;
   if (!out || !lse || !out_chunk || !lse_chunk || !status) return BD_ERR_ARG;
   if (!aligned16(out) || !aligned16(out_chunk)) return BD_ERR_ARG;
-  if (g.D == 512) return BD_ERR_ARG;  // the merge kernel takes D <= 256
   if (int rc = check_device()) return rc;
   return cuda_rc(launch_merge(g, out, lse, out_chunk, lse_chunk, status, static_cast<cudaStream_t>(stream)));
 }
@@ -293,13 +292,12 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* seg, const
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(seg)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
-  if (g.D == 512 && merge) return BD_ERR_ARG;  // the merging epilogue takes D <= 256
   CUtensorMap mq, mk, mv;
   if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map_kv(&mk, k, g, kTile) ||
       make_map_kv(&mv, v, g, kTile))
     return BD_ERR_CUDA;
   if (g.D == 512)
-    return cuda_rc(launch_fwd512(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status,
+    return cuda_rc(launch_fwd512(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status, merge,
                                  static_cast<cudaStream_t>(stream)));
   return cuda_rc(launch_fwd(mq, mk, mv, static_cast<const int32_t*>(seg), g, out, lse, status, merge,
                             static_cast<cudaStream_t>(stream)));

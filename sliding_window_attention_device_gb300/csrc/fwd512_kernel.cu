@@ -47,6 +47,9 @@ struct Fwd512Smem {
   int b, qt, kt_lo, nk, n_real, skip;
 };
 
+// kMerge: merge this K/V chunk's result into the running (out, lse) instead
+// of writing it (log-sum-exp weights, as the merge kernel).
+template <bool kMerge>
 __global__ void __launch_bounds__(kThreads512, 1)
     fwd512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
@@ -106,9 +109,11 @@ __global__ void __launch_bounds__(kThreads512, 1)
       const int i = qt * kTile + (tid - 128);
       if (i < g.L) {
         const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
-        uint4* o4 = reinterpret_cast<uint4*>(out + row * kD512);
-        for (int c = 0; c < kD512 / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        lse[row] = -INFINITY;
+        if (!kMerge || lse[row] == -INFINITY) {  // merging: a running result is kept
+          uint4* o4 = reinterpret_cast<uint4*>(out + row * kD512);
+          for (int c = 0; c < kD512 / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+          lse[row] = -INFINITY;
+        }
       }
     }
     return;
@@ -242,6 +247,11 @@ __global__ void __launch_bounds__(kThreads512, 1)
     const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
     const float sl2 = g.scale * 1.4426950408889634f;
     float m = -INFINITY, l = 0.f, nl2 = 0.f;  // nl2: -lse log2(e), pass 1
+    // what the epilogues write: out = w_new * (this chunk's normalised O)
+    // + w_old * (the running out) when merging; nothing for a row whose chunk
+    // result is empty while its running result is not
+    bool store = false;
+    float w_old = 0.f, w_new = 1.f;
     bool ok = true, empty = true;             // empty: the row sees no key at all
     int t = 0;
     for (int p = 0; p < 2 && ok; ++p) {
@@ -338,13 +348,26 @@ __global__ void __launch_bounds__(kThreads512, 1)
       if (ok && !warp_wait(&s.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &s.abort_flag, vstatus)) ok = false;
       if (!ok) break;
       tc_fence_after();
-      float scale_o = 1.0f;
+      float scale_o = w_new;  // pass 1: P was already normalised
       if (p == 0) {
         empty = !(real && l > 0.f);
-        const float lse_v = empty ? -INFINITY : (m + __log2f(l)) * 0.6931471805599453f;
-        if (i < g.L) lse[row] = lse_v;
-        nl2 = empty ? 0.f : -(m + __log2f(l));  // -lse log2(e)
-        scale_o = empty ? 0.f : 1.0f / l;
+        float lse_v = empty ? -INFINITY : (m + __log2f(l)) * 0.6931471805599453f;
+        nl2 = empty ? 0.f : -(m + __log2f(l));  // -lse log2(e) of this chunk
+        store = i < g.L;
+        if (kMerge && store) {
+          const float lse_o = lse[row];
+          if (lse_v == -INFINITY) {
+            store = lse_o == -INFINITY;  // nothing new: keep a running result, zero an empty one
+          } else if (lse_o != -INFINITY) {
+            const float mx = fmaxf(lse_o, lse_v);
+            const float ea = expf(lse_o - mx), eb = expf(lse_v - mx), tot = ea + eb;
+            w_old = ea / tot;
+            w_new = eb / tot;
+            lse_v = mx + logf(tot);
+          }
+        }
+        if (store) lse[row] = lse_v;
+        scale_o = empty ? 0.f : w_new / l;
       }
       uint4* o4 = reinterpret_cast<uint4*>(out + row * kD512 + 256 * p);
 #pragma unroll 1
@@ -352,12 +375,22 @@ __global__ void __launch_bounds__(kThreads512, 1)
         uint32_t o[32];
         tmem_ld32(t_o + c, o);
         tmem_wait_ld();
-        if (i < g.L) {
+        if (store) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float v[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = (p == 1 && empty) ? 0.f : __uint_as_float(o[8 * e + k]) * scale_o;
+            if (kMerge && w_old != 0.f) {  // an empty running side is not read
+              const uint4 old = o4[c / 8 + e];
+              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
+                v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
+                v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
+              }
+            }
             o4[c / 8 + e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                                        pack_bf16x2(v[6], v[7]));
           }
@@ -384,9 +417,10 @@ __global__ void __launch_bounds__(kThreads512, 1)
 
 }  // namespace
 
-// Forward for D = 512 (q, k, v maps with 64 x 128 boxes).
+// Forward for D = 512 (q, k, v maps with 64 x 128 boxes); `merge`: merged into
+// the running (out, lse).
 cudaError_t launch_fwd512(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
-                          const Geom& g, void* out, float* lse, int32_t* status, cudaStream_t st) {
+                          const Geom& g, void* out, float* lse, int32_t* status, bool merge, cudaStream_t st) {
   if (g.D != kD512) return cudaErrorInvalidValue;
   const size_t smem = sizeof(Fwd512Smem) + 1024;  // + 1 KB to align the swizzled tiles
   int dev = 0, max_optin = 0;
@@ -395,11 +429,12 @@ cudaError_t launch_fwd512(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(fwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kern = merge ? fwd512_kernel<true> : fwd512_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * g.Hq;  // (q tile, query head)
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (const cudaError_t le = launch_pdl(fwd512_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads512), smem,
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads512), smem,
       st, mq, mk, mv, seg, g, static_cast<__nv_bfloat16*>(out), lse, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }

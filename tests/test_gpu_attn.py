@@ -1,7 +1,7 @@
 """Forward / backward parity of the CUDA path against the fp64 oracle, element by
 element, at sizes the oracle finishes in seconds: several 128-row tiles, ragged
-q and K/V tails, odd and even GQA groups, D = 64 / 128 / 256, windows, K/V
-sub-ranges, all-padding shards and length-1 documents."""
+q and K/V tails, odd and even GQA groups, D = 64 / 128 / 256 / 512, windows,
+K/V sub-ranges, all-padding shards and length-1 documents."""
 import numpy as np
 import pytest
 import torch
@@ -32,6 +32,10 @@ CASES = [
     ("d128_window1", W("h", 1, 2, 1, 128, 512, 2, ("uniform", 30, 200, 5), window=1), (1,)),
     ("d64_g4_big_window", W("i", 2, 8, 2, 64, 1024, 4, ("uniform", 60, 500, 90), window=100000), (1, 2)),
     ("d128_all_pad_shard", W("j", 1, 2, 1, 128, 1024, 4, ("explicit", (300, 200), 524)), (2, 3, 1)),
+    ("d512_g2_needed", W("k", 1, 4, 2, 512, 1024, 4, ("uniform", 30, 400, 20), kv="needed"), (1, 3)),
+    ("d512_len1_docs", W("l", 1, 2, 1, 512, 640, 2, ("uniform", 1, 3, 17)), (0,)),
+    ("d512_window1", W("m", 1, 2, 1, 512, 512, 2, ("uniform", 30, 200, 5), window=1), (1,)),
+    ("d512_all_pad_shard", W("n", 1, 2, 1, 512, 1024, 4, ("explicit", (300, 200), 524)), (2, 3)),
 ]
 
 

@@ -32,6 +32,8 @@ CASES = [
                      layout=("uniform", 50, 400, 70), window=100), 1, (0, 128, 517, None)),
     ("d256_window", W("cc", "chunked, D 256, window 150", B=1, Hq=4, Hkv=2, D=256, S=1280, cp_size=4,
                       layout=("uniform", 100, 600, 30), window=150, kv="prefix"), 3, (0, 830, 1000, None)),
+    ("d512_prefix", W("cd", "chunked, D 512, GQA 2", B=1, Hq=4, Hkv=2, D=512, S=1024, cp_size=4,
+                      layout=("uniform", 60, 500, 20), kv="prefix"), 2, (0, 300, 700, None)),
 ]
 
 
@@ -135,16 +137,17 @@ def test_chunked_forward_merge_and_backward(name, w, r, edges):
         assert (dks[-1] == 0).all() and (dvs[-1] == 0).all()
 
 
-def test_merge_edge_cases():
+@pytest.mark.parametrize("D", [64, 512])
+def test_merge_edge_cases(D):
     """Both sides empty stays (0, -inf); an empty side is the identity even
     when its out is not finite; merging equal lse gives the average."""
     from sliding_window_attention_device_gb300 import bdattn
     dev = torch.device("cuda")
-    g = bdattn.geom(1, 2, 1, 64, 256, 128, 0, 0, 256, 0)
+    g = bdattn.geom(1, 2, 1, D, 256, 128, 0, 0, 256, 0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     gen = torch.Generator(device="cpu").manual_seed(5)
-    a = torch.randn(1, 2, 128, 64, generator=gen).to(torch.bfloat16)
-    b = torch.randn(1, 2, 128, 64, generator=gen).to(torch.bfloat16)
+    a = torch.randn(1, 2, 128, D, generator=gen).to(torch.bfloat16)
+    b = torch.randn(1, 2, 128, D, generator=gen).to(torch.bfloat16)
     la = torch.randn(1, 2, 128, generator=gen) * 3
     lb = torch.randn(1, 2, 128, generator=gen) * 3
     # rows 0..31: a empty; 32..63: b empty; 64..95: both empty; 96..127: equal lse
@@ -171,7 +174,8 @@ def test_merge_edge_cases():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key,r,fused", [("C2", 3, True), ("C2", 7, False), ("C3", 7, True), ("C5w512", 5, True)])
+@pytest.mark.parametrize("key,r,fused", [("C2", 3, True), ("C2", 7, False), ("C3", 7, True), ("C5w512", 5, True),
+                                         ("G512", 6, True)])
 def test_ring_chunks_full_size_sampled(key, r, fused):
     """Full size, through the chunking and calls the benchmark's ring modes time
     (merges in the forward's epilogue, or by the merge kernel):

@@ -8,8 +8,9 @@ on the GPU against the oracle:
     CTAs per K/V tile, S and dP formed in each): fp32 and bf16 gradients;
   * several q tiles with a ragged tail, GQA, a window, token-major K/V, and
     sampled rows / keys of the full-size workload.
-The entry points without a D = 512 path (the merging epilogue, the fixed-order
-backward) refuse it."""
+(Chunked K/V with merges at D = 512 is covered with the other head dims in
+the chunked-path tests.) The fixed-order backward has no D = 512 path and
+refuses it."""
 import numpy as np
 import pytest
 import torch
@@ -96,12 +97,10 @@ def test_d512_backward_bf16_gradients():
         assert (a.float() - b_).abs().max().item() <= tol, n
 
 
-def test_d512_refused_where_unbuilt():
+def test_d512_deterministic_refused():
     from sliding_window_attention_device_gb300 import bdattn
     c = make_case(CASES[0][1], CASES[0][2])
     g, seg, status, out, lse, (q, k, v, _) = _fwd(c, 0)
-    with pytest.raises(RuntimeError):
-        bdattn.bd_attn_fwd_merge(q, k, v, seg, g, status, out, lse)
     with pytest.raises(RuntimeError):
         bdattn.bd_attn_bwd_deterministic(c["do"].cuda(), q, k, v, out, lse, seg, g, status)
 
