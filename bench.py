@@ -599,7 +599,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
-        "roofline": {"kernel": (f"backward: delta, zero-fill, bwd128_kernel<{w.D}> without dq, bwd_dq_kernel<{w.D}>"
+        "roofline": {"kernel": (f"backward: delta, zero-fill, {BWD_KERNEL[w.D]} without dq, "
+                                f"{'bwd_dq256_kernel' if w.D == 256 else f'bwd_dq_kernel<{w.D}>'}"
                                 if getattr(rep, "deterministic", False) else
                                 f"{BWD_KERNEL[w.D]} (backward main stage, with its dK/dV zero-fill launch)"),
                      "bound": "tensor", "achieved": round(bwd_achieved, 2),

@@ -216,8 +216,9 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
  * query head walks its K/V tiles in increasing order, recomputing S and dP and
  * accumulating dQ in tensor memory -- no atomic additions anywhere. Same
  * arguments and results as bd_attn_bwd (workspace: the same size, holding
- * delta); D must be 64 or 128 (BD_ERR_ARG otherwise). Three launches: delta,
- * zero-fill + dK / dV, dq. */
+ * delta); D must be 64, 128 or 256 (BD_ERR_ARG otherwise; at D = 256 the dq
+ * pass streams each K/V tile's K twice, for S and for dQ). Three launches:
+ * delta, zero-fill + dK / dV, dq. */
 int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, const void* v, const void* out,
                               const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq,
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream);

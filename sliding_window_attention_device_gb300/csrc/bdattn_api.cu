@@ -398,7 +398,7 @@ int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, co
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D != 64 && g.D != 128) return BD_ERR_ARG;
+  if (g.D != 64 && g.D != 128 && g.D != 256) return BD_ERR_ARG;
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
@@ -407,15 +407,18 @@ int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, co
     return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
   if (!load_encode()) return BD_ERR_CUDA;
-  CUtensorMap mq, mdo, mk, mv;
+  // the dq pass reads 128-row q / dout boxes; the dK / dV kernel's boxes follow its head dim
+  CUtensorMap mq, mdo, mk, mv, mq_m, mdo_m;
+  const int qbox = bwd_q_box_rows(g.D);
   if (make_map(&mq, q, g.D, g.L, g.B * g.Hq, kTile) || make_map(&mdo, dout, g.D, g.L, g.B * g.Hq, kTile) ||
+      make_map(&mq_m, q, g.D, g.L, g.B * g.Hq, qbox) || make_map(&mdo_m, dout, g.D, g.L, g.B * g.Hq, qbox) ||
       make_map_kv(&mk, k, g, kTile) || make_map_kv(&mv, v, g, kTile))
     return BD_ERR_CUDA;
   const auto st = static_cast<cudaStream_t>(stream);
   const int32_t* sg = static_cast<const int32_t*>(seg);
   const int bf16 = grad_dtype == BD_DTYPE_BF16;
   if (int rc = cuda_rc(launch_bwd_delta(g, dout, out, workspace, status, st))) return rc;
-  if (int rc = cuda_rc(launch_bwd_main_nodq(mq, mdo, mk, mv, sg, g, lse, dk, dv, bf16, workspace, status, st)))
+  if (int rc = cuda_rc(launch_bwd_main_nodq(mq_m, mdo_m, mk, mv, sg, g, lse, dk, dv, bf16, workspace, status, st)))
     return rc;
   return cuda_rc(launch_bwd_dq(mq, mdo, mk, mv, sg, g, lse, bwd_delta_ptr(g, workspace), dq, bf16, status, st));
 }

@@ -163,7 +163,8 @@ constexpr int kBwdThreads = 512;
 constexpr int kBwdModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
 constexpr int kBwdModeWork = 1;  // an attended K/V tile
 
-template <int D>
+// kDq: with the dq products (else dK / dV only, for the fixed-order dq pass).
+template <int D, bool kDq>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -423,15 +424,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int ks = 0; ks < kBwdQ / 16; ++ks)
           umma_ss(tbase + Cfg::kColDk, desc_at(dK_major, a_ds + ks * 32), desc_at(dMN_q, a_q + pass_off_q + ks * 2048),
                   idDKV, (!first_of_pass || ks > 0) ? 1u : 0u);
-        const int bq = it & 1;  // dQ^T tensor-memory buffer
-        if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t a_kpass = a_k + pass * (kDp / 64) * Smem::kKChunk;
+        if constexpr (kDq) {
+          const int bq = it & 1;  // dQ^T tensor-memory buffer
+          if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_kpass = a_k + pass * (kDp / 64) * Smem::kKChunk;
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ss(tbase + Cfg::kColDq + 64 * bq, desc_at(dMN_k, a_kpass + ks * 2048), desc_at(dMN_k, a_ds + ks * 2048),
-                  idDQ, ks > 0 ? 1u : 0u);
-        umma_commit(&s.dq_full[bq]);
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_ss(tbase + Cfg::kColDq + 64 * bq, desc_at(dMN_k, a_kpass + ks * 2048),
+                    desc_at(dMN_k, a_ds + ks * 2048), idDQ, ks > 0 ? 1u : 0u);
+          umma_commit(&s.dq_full[bq]);
+        }
         umma_commit(&s.ds_empty);
         umma_commit(&s.grp_empty[pass]);  // this pass's group: read by dV, dK above
         if (last_of_pass) umma_commit(&s.acc_full);
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the pass == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -678,13 +681,13 @@ unsigned grid_for(long long work_items) {
   return static_cast<unsigned>(blocks < 152 * 16 ? (blocks > 0 ? blocks : 1) : 152 * 16);
 }
 
-template <int D>
+template <int D, bool kDq>
 cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdq, const int32_t* seg, const Geom& g, const float* lse,
                           const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
                           cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem<D, BwdCfg<D>::kNsq>) + 1024;  // + 1 KB to align the swizzled tiles
-  auto kern = bwd_kernel<D>;
+  auto kern = bwd_kernel<D, kDq>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // only tiles some local row can reach by position get a working CTA; with
@@ -786,23 +789,27 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
       return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 256:
-      return launch_main_d<256>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+      return launch_main_d<256, true>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 512:  // the head dim of the outputs split over four CTAs (bwd512_kernel.cu)
       return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-// K4 without the dq products (D = 64 / 128): dK, dV and the zero-fill only,
-// for the fixed-order dq pass.
+// K4 without the dq products (D = 64 / 128 / 256; for D = 256 the q / dout
+// maps have kBwdQ-row boxes): dK, dV and the zero-fill only, for the
+// fixed-order dq pass.
 cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                  const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                  void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
-  if (g.D != 64 && g.D != 128) return cudaErrorInvalidValue;
+  if (g.D != 64 && g.D != 128 && g.D != 256) return cudaErrorInvalidValue;
   const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
   const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
   if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
       status); le != cudaSuccess) return le;
+  if (g.D == 256)  // the dq map is not read without the dq products
+    return launch_main_d<256, false>(mq, mdo, mk, mv, mq, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16,
+                                     status, st);
   return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
                             st);
 }

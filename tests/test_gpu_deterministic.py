@@ -5,8 +5,9 @@ products, dq from the fixed-order pass) on the GPU:
   * two runs give identical dq, dk and dv, bit for bit;
   * dk / dv equal those of the atomic-add backward bit for bit (the same
     arithmetic), and dq matches it within the parity tolerance;
-  * dq, dk, dv match the oracle (windows, ragged tails, D = 64 / 128, GQA,
-    token-major K/V, bf16 gradients, and sampled rows of full-size workloads).
+  * dq, dk, dv match the oracle (windows, ragged tails, D = 64 / 128 / 256,
+    GQA, token-major K/V, bf16 gradients, and sampled rows of full-size
+    workloads).
 """
 import numpy as np
 import pytest
@@ -26,6 +27,10 @@ CASES = [
                          layout=("uniform", 50, 400, 70), window=100), 1, 0),
     ("d128_window_prefix_tm", W_("dc", "deterministic, D 128, window 150, token-major", B=1, Hq=4, Hkv=2, D=128,
                                  S=1280, cp_size=4, layout=("uniform", 100, 600, 30), window=150, kv="prefix"), 3, 1),
+    ("d256_g2_window", W_("dd", "deterministic, D 256, window 300", B=1, Hq=4, Hkv=2, D=256, S=1280, cp_size=4,
+                          layout=("uniform", 100, 600, 30), window=300, kv="prefix"), 3, 0),
+    ("d256_ragged_tm", W_("de", "deterministic, D 256, ragged, token-major", B=2, Hq=2, Hkv=1, D=256, S=1024,
+                          cp_size=4, layout=("uniform", 20, 300, 40)), 2, 1),
 ]
 
 
@@ -86,7 +91,7 @@ def test_deterministic_bf16_gradients():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("key,r", [("C2", 4), ("C5w512", 3)])
+@pytest.mark.parametrize("key,r", [("C2", 4), ("C5w512", 3), ("C3", 7)])
 def test_deterministic_full_size_sampled(key, r):
     from sliding_window_attention_device_gb300 import bdattn
     from test_gpu_full import _check, _oracle_sampled, _pick
