@@ -57,6 +57,8 @@ UNIT = "TFLOP/s"
 # the backward main-stage kernel of each head dim
 BWD_KERNEL = {64: "bwd128_kernel<64>", 128: "bwd128_kernel<128>", 256: "bwd_kernel<256>",
               512: "bwd512_kernel (four CTAs per K/V tile, one per 128-column slice)"}
+# the fixed-order dq pass of each head dim above 128
+DQ_KERNEL = {256: "bwd_dq256_kernel", 512: "bwd_dq512_kernel (two CTAs per q tile, one per 256-column half)"}
 TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "cd9d083444a3a85a", "bytes_per_launch": 1.16909e9}
 
 
@@ -600,7 +602,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
         "roofline": {"kernel": (f"backward: delta, zero-fill, {BWD_KERNEL[w.D]} without dq, "
-                                f"{'bwd_dq256_kernel' if w.D == 256 else f'bwd_dq_kernel<{w.D}>'}"
+                                f"{DQ_KERNEL.get(w.D, f'bwd_dq_kernel<{w.D}>')}"
                                 if getattr(rep, "deterministic", False) else
                                 f"{BWD_KERNEL[w.D]} (backward main stage, with its dK/dV zero-fill launch)"),
                      "bound": "tensor", "achieved": round(bwd_achieved, 2),

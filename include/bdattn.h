@@ -32,9 +32,8 @@
  *   lse      fp32  [B, Hq,  L]        natural-log sum-exp; -inf on padding rows
  *   dq       fp32 or bf16 [B, Hq, L, D]
  *   dk, dv   fp32 or bf16 [B, Hkv, S_kv, D]   summed over each GQA group (k's layout)
- * D must be 64, 128, 256 or 512 (the head-dim-512 global layers of
- * gemma4_moe.cp_attention; for D = 512 the fixed-order backward returns
- * BD_ERR_ARG). All device pointers are caller-owned and must be
+ * D must be 64, 128, 256 or 512 (512: the head-dim-512 global layers of
+ * gemma4_moe.cp_attention). All device pointers are caller-owned and must be
  * 16-byte aligned. The library allocates no device memory and never
  * synchronises the stream; every entry point only enqueues work on `stream`.
  *
@@ -216,9 +215,10 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
  * query head walks its K/V tiles in increasing order, recomputing S and dP and
  * accumulating dQ in tensor memory -- no atomic additions anywhere. Same
  * arguments and results as bd_attn_bwd (workspace: the same size, holding
- * delta); D must be 64, 128 or 256 (BD_ERR_ARG otherwise; at D = 256 the dq
- * pass streams each K/V tile's K twice, for S and for dQ). Three launches:
- * delta, zero-fill + dK / dV, dq. */
+ * delta); any head dim (at D = 256 the dq pass streams each K/V tile's K
+ * twice, for S and for dQ; at D = 512 two CTAs per q tile and query head each
+ * form S and dP for one 256-column half of dq). Three launches: delta,
+ * zero-fill + dK / dV, dq. */
 int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, const void* v, const void* out,
                               const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq,
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream);

@@ -308,7 +308,7 @@ def bd_attn_bwd(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.
 
 def bd_attn_bwd_deterministic(dout, q, k, v, out, lse, seg, g: Geom, status, grad_dtype=torch.float32, dq=None,
                               dk=None, dv=None, workspace=None, stream=None):
-    """bd_attn_bwd with bitwise reproducible results (dq by a fixed-order pass; D = 64, 128 or 256)."""
+    """bd_attn_bwd with bitwise reproducible results (dq by a fixed-order pass)."""
     return bd_attn_bwd(dout, q, k, v, out, lse, seg, g, status, grad_dtype, dq, dk, dv, workspace, stream,
                        _fn="bd_attn_bwd_deterministic")
 

@@ -398,7 +398,6 @@ int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, co
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.D != 64 && g.D != 128 && g.D != 256) return BD_ERR_ARG;
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;

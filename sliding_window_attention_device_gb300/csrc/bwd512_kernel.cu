@@ -75,6 +75,8 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 // Chunk index (of the eight 64-column chunks) of the i-th streamed chunk of slice c.
 __device__ __forceinline__ int streamed_chunk(int c, int i) { return i < 2 * c ? i : i + 2; }
 
+// kDq: with the dq products (else dK / dV only, for the fixed-order dq pass).
+template <bool kDq>
 __global__ void __launch_bounds__(kThreads5, 1)
     bwd512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -321,17 +323,19 @@ __global__ void __launch_bounds__(kThreads5, 1)
         for (int ks = 0; ks < kBwdQ / 16; ++ks)
           umma_ss(tbase + kColDk, desc_at(dK_major, a_ds + ks * 32), desc_at(dMN_q, a_qs + ks * 2048), idDKV,
                   (it > 0 || ks > 0) ? 1u : 0u);
-        const int bq = it & 1;  // dQ^T tensor-memory buffer
-        if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        if constexpr (kDq) {
+          const int bq = it & 1;  // dQ^T tensor-memory buffer
+          if (it >= 2 && !wait(&s.dq_empty[bq], ((it >> 1) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks)
-          umma_ss(tbase + kColDq + 64 * bq, desc_at(dMN_k, a_kc + ks * 2048), desc_at(dMN_k, a_ds + ks * 2048), idDQ,
-                  ks > 0 ? 1u : 0u);
-        umma_commit(&s.dq_full[bq]);
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_ss(tbase + kColDq + 64 * bq, desc_at(dMN_k, a_kc + ks * 2048), desc_at(dMN_k, a_ds + ks * 2048),
+                    idDQ, ks > 0 ? 1u : 0u);
+          umma_commit(&s.dq_full[bq]);
+        }
         umma_commit(&s.ds_empty);
         umma_commit(&s.qs_empty);
         if (it == n_it - 1) umma_commit(&s.acc_full);
@@ -494,7 +498,7 @@ __global__ void __launch_bounds__(kThreads5, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
-  } else if (warp >= 8 && warp < 12) {
+  } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the slice == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -544,18 +548,20 @@ __global__ void __launch_bounds__(kThreads5, 1)
 // K4e launch: one CTA per (attended K/V tile, kv head, 128-column slice), the
 // four slices of a tile adjacent in the grid; only tiles some local row can
 // reach by position get CTAs (the zero-fill kernel writes the others' zeros).
+// Without a dq accumulator (dq_acc null) the dq products are left out.
 cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
                                cudaStream_t st) {
   if (g.D != kD5) return cudaErrorInvalidValue;
   const size_t smem = sizeof(Bwd512Smem) + 1024;  // + 1 KB to align the swizzled tiles
-  cudaError_t e = cudaFuncSetAttribute(bwd512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kern = dq_acc ? bwd512_kernel<true> : bwd512_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int reach = kv_tiles_reachable(g);
   const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv * kNSlice;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (const cudaError_t le = launch_pdl(bwd512_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads5), smem, st,
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads5), smem, st,
       mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }

@@ -796,17 +796,20 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
   }
 }
 
-// K4 without the dq products (D = 64 / 128 / 256; for D = 256 the q / dout
-// maps have kBwdQ-row boxes): dK, dV and the zero-fill only, for the
+// K4 without the dq products (D = 64 / 128 / 256 / 512; for D >= 256 the
+// q / dout maps have kBwdQ-row boxes): dK, dV and the zero-fill only, for the
 // fixed-order dq pass.
 cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                  const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                  void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
-  if (g.D != 64 && g.D != 128 && g.D != 256) return cudaErrorInvalidValue;
+  if (g.D != 64 && g.D != 128 && g.D != 256 && g.D != 512) return cudaErrorInvalidValue;
   const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
   const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
   if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
       status); le != cudaSuccess) return le;
+  if (g.D == 512)
+    return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
+                              st);
   if (g.D == 256)  // the dq map is not read without the dq products
     return launch_main_d<256, false>(mq, mdo, mk, mv, mq, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16,
                                      status, st);

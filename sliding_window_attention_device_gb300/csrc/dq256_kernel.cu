@@ -19,7 +19,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
-#include "pipeline.cuh"
+#include "dq_stream.cuh"
 
 namespace bd {
 
@@ -239,8 +239,6 @@ __global__ void __launch_bounds__(kThreads256, 1)
       nl2 = lse[row0 + i] * -1.4426950408889634f;
       ndl = delta[row0 + i] * -g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
     }
-    const float2 sl2 = make_float2(g.scale * 1.4426950408889634f, g.scale * 1.4426950408889634f);
-    const float2 sc = make_float2(g.scale, g.scale), nl2v = make_float2(nl2, nl2), ndlv = make_float2(ndl, ndl);
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
       if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, vstatus)) {
@@ -252,35 +250,9 @@ __global__ void __launch_bounds__(kThreads256, 1)
       // a row sees all of this tile, none of it, or part of it
       const bool dead = !real || jhi < c0 || jlo > c0 + kTile - 1;
       const bool full = jlo <= c0 && c0 + kTile - 1 <= jhi;
-      const int a_lo = jlo - c0, e_hi = jhi - c0;
       uint32_t pk[2][32];  // dS of keys [64 hf, 64 hf + 64), bf16 pairs
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[64], dr[64];
-        tmem_ld32(tbase + lane_off + kColS + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tbase + lane_off + kColS + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld32(tbase + lane_off + kColDp + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-        tmem_ld32(tbase + lane_off + kColDp + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-        tmem_wait_ld();
-        tmem_regs_ready<64>(sr);
-        tmem_regs_ready<64>(dr);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = 64 * hf + 2 * e;
-          const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), sl2, nl2v);
-          float p0 = fast_exp2(t.x), p1 = fast_exp2(t.y);
-          if (dead) {
-            p0 = 0.f;
-            p1 = 0.f;
-          } else if (!full) {
-            p0 = (c >= a_lo && c <= e_hi) ? p0 : 0.f;
-            p1 = (c + 1 >= a_lo && c + 1 <= e_hi) ? p1 : 0.f;
-          }
-          const float2 d = __ffma2_rn(make_float2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), sc, ndlv);
-          const float2 ds = __fmul2_rn(make_float2(p0, p1), d);
-          pk[hf][e] = pack_bf16x2(ds.x, ds.y);
-        }
-      }
+      dq_form_ds(tbase + lane_off + kColS, tbase + lane_off + kColDp, g.scale, nl2, ndl, dead, full, jlo - c0,
+                 jhi - c0, pk);
       // dS over this row's S columns (read above): the A operand of the dQ products
       tmem_st32(tbase + lane_off + kColS, pk[0]);
       tmem_st32(tbase + lane_off + kColS + 32, pk[1]);
@@ -295,28 +267,7 @@ __global__ void __launch_bounds__(kThreads256, 1)
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     } else {
       tc_fence_after();
-      const size_t row = row0 + i;
-#pragma unroll 1
-      for (int c = 0; c < kD256; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tbase + lane_off + kColDq + c, o);
-        tmem_wait_ld();
-        if (i < g.L) {
-          if (dq_bf16) {
-            uint4* d4 = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dq) + row * kD256 + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * e]), __uint_as_float(o[8 * e + 1])),
-                                 pack_bf16x2(__uint_as_float(o[8 * e + 2]), __uint_as_float(o[8 * e + 3])),
-                                 pack_bf16x2(__uint_as_float(o[8 * e + 4]), __uint_as_float(o[8 * e + 5])),
-                                 pack_bf16x2(__uint_as_float(o[8 * e + 6]), __uint_as_float(o[8 * e + 7])));
-          } else {
-            uint4* d4 = reinterpret_cast<uint4*>(static_cast<float*>(dq) + row * kD256 + c);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) d4[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
-          }
-        }
-      }
+      dq_store_cols(tbase + lane_off + kColDq, kD256, dq, (row0 + i) * kD256, dq_bf16, i < g.L);
     }
   }
 

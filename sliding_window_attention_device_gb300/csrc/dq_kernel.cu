@@ -368,8 +368,11 @@ cudaError_t launch_dq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
 cudaError_t launch_bwd_dq256(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                              const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                              const float* delta, void* dq, int bf16, int32_t* status, cudaStream_t st);
+cudaError_t launch_bwd_dq512(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
+                             const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
+                             const float* delta, void* dq, int bf16, int32_t* status, cudaStream_t st);
 
-// dq in a fixed order for D = 64 / 128 / 256 (q and dout maps with 128-row boxes).
+// dq in a fixed order for D = 64 / 128 / 256 / 512 (q and dout maps with 128-row boxes).
 cudaError_t launch_bwd_dq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                           const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                           const float* delta, void* dq, int bf16, int32_t* status, cudaStream_t st) {
@@ -377,6 +380,7 @@ cudaError_t launch_bwd_dq(const CUtensorMap& mq, const CUtensorMap& mdo, const C
     case 64: return launch_dq<64, 3>(mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status, st);
     case 128: return launch_dq<128, 2>(mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status, st);
     case 256: return launch_bwd_dq256(mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status, st);  // dq256_kernel.cu
+    case 512: return launch_bwd_dq512(mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status, st);  // dq512_kernel.cu
     default: return cudaErrorInvalidValue;
   }
 }

@@ -121,7 +121,7 @@ def test_kv_layout_constants_and_validation(lib):
     assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
 
 
-def test_deterministic_backward_rejects_d512(lib):
+def test_deterministic_backward_rejects_null_pointers(lib):
     g = bdattn.geom(1, 2, 1, 512, 256, 64, 0, 0, 256, 0)
     assert lib.bd_attn_bwd_deterministic(None, None, None, None, None, None, None, ctypes.byref(g), 0, None, None,
                                          None, None, None, None) == bdattn.BD_ERR_ARG

@@ -8,9 +8,9 @@ on the GPU against the oracle:
     CTAs per K/V tile, S and dP formed in each): fp32 and bf16 gradients;
   * several q tiles with a ragged tail, GQA, a window, token-major K/V, and
     sampled rows / keys of the full-size workload.
+  * the bitwise reproducible backward (two-half fixed-order dq pass).
 (Chunked K/V with merges at D = 512 is covered with the other head dims in
-the chunked-path tests.) The fixed-order backward has no D = 512 path and
-refuses it."""
+the chunked-path tests.)"""
 import numpy as np
 import pytest
 import torch
@@ -97,12 +97,33 @@ def test_d512_backward_bf16_gradients():
         assert (a.float() - b_).abs().max().item() <= tol, n
 
 
-def test_d512_deterministic_refused():
+@pytest.mark.parametrize("name,w,r,layout", CASES[:2], ids=[x[0] for x in CASES[:2]])
+def test_d512_deterministic(name, w, r, layout):
+    """The bitwise reproducible backward at D = 512 (dK / dV from the main
+    kernel without its dq products, dq from the two-half fixed-order pass):
+    two runs agree bit for bit, dK / dV equal the atomic backward's, and all
+    three match the oracle."""
     from sliding_window_attention_device_gb300 import bdattn
-    c = make_case(CASES[0][1], CASES[0][2])
-    g, seg, status, out, lse, (q, k, v, _) = _fwd(c, 0)
-    with pytest.raises(RuntimeError):
-        bdattn.bd_attn_bwd_deterministic(c["do"].cuda(), q, k, v, out, lse, seg, g, status)
+    c = make_case(w, r)
+    g, seg, status, out, lse, qkv = _fwd(c, layout)
+    q, k, v, _ = qkv
+    runs = []
+    for _ in range(2):
+        dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.float32, device=q.device)
+        dk = torch.full(bdattn.kv_shape(g), float("nan"), dtype=torch.float32, device=q.device)
+        dv = torch.full_like(dk, float("nan"))
+        bdattn.bd_attn_bwd_deterministic(c["do"].to(q.device), q, k, v, out, lse, seg, g, status, dq=dq, dk=dk, dv=dv)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        runs.append((dq.cpu(), dk.cpu(), dv.cpu()))
+    for x, y, n in zip(runs[0], runs[1], ("dq", "dk", "dv")):
+        assert torch.equal(x, y), f"{name}: {n} differs between two runs"
+    adq, adk, adv = _bwd(c, g, seg, status, out, lse, qkv, layout)
+    assert torch.equal(runs[0][1], adk) and torch.equal(runs[0][2], adv)
+    rdq, rdk, rdv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], oracle_geom(c))
+    assert_close(f"{name} deterministic dq", runs[0][0], rdq)
+    assert_close(f"{name} deterministic dk", runs[0][1], rdk)
+    assert_close(f"{name} deterministic dv", runs[0][2], rdv)
 
 
 @pytest.mark.slow
