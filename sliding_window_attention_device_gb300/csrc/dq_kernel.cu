@@ -13,7 +13,8 @@
 //   warp 0   TMA: Q and dO once, K / V tiles through an NS-stage ring
 //   warp 1   one thread issues the MMAs       warp 2  tensor memory
 //   warps 4-7  thread = q row: P, dS, and the dq rows at the end
-// D = 64 or 128 (S, dP and dQ fill 384 of the 512 tensor-memory columns).
+// D = 64 or 128 (S, dP and dQ fill 384 of the 512 tensor-memory columns);
+// D = 256 and 512 stream K/V through a chunk ring (dq256_kernel.cu, dq512_kernel.cu).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
