@@ -97,7 +97,7 @@ def test_d512_backward_bf16_gradients():
         assert (a.float() - b_).abs().max().item() <= tol, n
 
 
-@pytest.mark.parametrize("name,w,r,layout", CASES[:2], ids=[x[0] for x in CASES[:2]])
+@pytest.mark.parametrize("name,w,r,layout", CASES, ids=[x[0] for x in CASES])
 def test_d512_deterministic(name, w, r, layout):
     """The bitwise reproducible backward at D = 512 (dK / dV from the main
     kernel without its dq products, dq from the two-half fixed-order pass):
@@ -115,7 +115,8 @@ def test_d512_deterministic(name, w, r, layout):
         bdattn.bd_attn_bwd_deterministic(c["do"].to(q.device), q, k, v, out, lse, seg, g, status, dq=dq, dk=dk, dv=dv)
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        runs.append((dq.cpu(), dk.cpu(), dv.cpu()))
+        back = (lambda t: t.permute(1, 2, 0, 3)) if layout else (lambda t: t)  # token-major: to [B, Hkv, S_kv, D]
+        runs.append((dq.cpu(), back(dk).cpu(), back(dv).cpu()))
     for x, y, n in zip(runs[0], runs[1], ("dq", "dk", "dv")):
         assert torch.equal(x, y), f"{name}: {n} differs between two runs"
     adq, adk, adv = _bwd(c, g, seg, status, out, lse, qkv, layout)
