@@ -75,6 +75,23 @@ def test_bad_geometry_rejected(lib, bad):
     assert rc == bdattn.BD_ERR_ARG
 
 
+@pytest.mark.parametrize("D", [32, 96, 384, 1024])
+def test_unsupported_head_dims_rejected(lib, D):
+    g = bdattn.geom(1, 2, 1, D, 256, 64, 0, 0, 256)
+    assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
+    assert lib.bd_attn_bwd_workspace_bytes(ctypes.byref(g)) == 0
+
+
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+def test_every_head_dim_has_sizes(lib, D):
+    """Every mode runs at every supported head dim: the table and the backward
+    workspace (fp32 dq accumulator + delta) are sized for it."""
+    g = bdattn.geom(1, 4, 2, D, 1024, 256, 256, 0, 1024)
+    assert lib.bd_attn_seg_bytes(ctypes.byref(g)) > 0
+    rows = 4 * 256
+    assert lib.bd_attn_bwd_workspace_bytes(ctypes.byref(g)) >= rows * D * 4 + rows * 4
+
+
 def test_null_pointers_rejected(lib):
     g = bdattn.geom(1, 2, 1, 64, 256, 64, 128, 0, 256)
     P = ctypes.c_void_p
