@@ -127,6 +127,20 @@ def read_peaks() -> dict:
     return dict(source="fallback", bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, hbm_gbs=6800.0)
 
 
+def choose_peak(peaks: dict, clocks: dict) -> tuple[float, str]:
+    """The bf16 denominator that matches the clock record of the timed region:
+    the burst figure (a GEMM timed alone at full clock) when the median SM
+    clock sat at its maximum and the power cap never engaged, else the
+    sustained one (a GEMM held for seconds under the power cap)."""
+    burst, sust = peaks.get("bf16_tflops"), peaks.get("bf16_tflops_sustained")
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    at_max = sm is not None and bool(smax) and sm >= 0.99 * smax
+    if burst and (at_max and not capped or not sust):
+        return float(burst), f"{peaks['source']} bf16_tflops (burst: median SM clock at its maximum, no power cap)"
+    return float(sust), f"{peaks['source']} bf16_tflops_sustained (SM clock below its maximum or power-capped)"
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -514,6 +528,92 @@ def run_exchange(args, local_rank: int) -> dict:
     }
 
 
+def smi_index(local_rank: int) -> str:
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    return visible[local_rank].strip() if local_rank < len(visible) else str(local_rank)
+
+
+def timed_steps(rep, steps: int, warmup: int, world: int, local_rank: int) -> dict:
+    """W untimed warm-up steps, then exactly `steps` steps between two CUDA events on
+    the launching stream, bracketed by a barrier and a synchronize on both sides,
+    with per-shard forward / backward events and the SM clocks sampled meanwhile."""
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(warmup):
+        rep.step()
+    torch.cuda.synchronize()
+    if int(rep.status.item()) != 0:
+        raise RuntimeError(f"device status {int(rep.status.item()):#x} after warm-up")
+    n = len(rep.shards)
+    ev_steps = [{"fwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
+                 "bwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
+                 "merge": []}
+                for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(smi_index(local_rank)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(steps):
+            rep.step(ev_steps[k])
+        stop.record()
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    if int(rep.status.item()) != 0:
+        raise RuntimeError(f"device status {int(rep.status.item()):#x} in the timed region")
+    fwd_only = getattr(rep, "fwd_only", False)
+    return {
+        "ms": start.elapsed_time(stop),
+        "fwd_ms": sum(e["fwd"][i][0].elapsed_time(e["fwd"][i][1]) for e in ev_steps for i in range(n)),
+        "bwd_ms": 0.0 if fwd_only else sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1])
+                                           for e in ev_steps for i in range(n)),
+        "merge_ms": sum(a.elapsed_time(b) for e in ev_steps for a, b in e["merge"]),
+        "n_merge": sum(len(e["merge"]) for e in ev_steps),
+        "clocks": clocks,
+    }
+
+
+# the other workloads timed in the same run as the headline (few steps each)
+OTHER_CONFIGS = (("C3", None), ("C4", {15}), ("C5w512", None), ("G512", None))
+
+
+def run_other_configs(args, dev, local_rank: int, peaks: dict) -> dict:
+    """fwd+bwd throughput of the other workloads, same fields and timing rules as
+    the headline line (CUDA events, inputs resident, clock record per workload)."""
+    res = {}
+    grad_dtype = torch.bfloat16 if args.grad_dtype == "bf16" else torch.float32
+    steps, warmup = max(3, min(args.steps, 5)), 3
+    for key, ranks in OTHER_CONFIGS:
+        w = synth.WORKLOADS[key]
+        rep = Replica(w, args.seed, dev, grad_dtype, ranks)
+        total_flop, fwd_flop, bwd_flop = rep.flops()
+        t = timed_steps(rep, steps, warmup, 1, local_rank)
+        ms_per_step = t["ms"] / steps
+        value = total_flop / (ms_per_step * 1e-3) / 1e12
+        bwd_tf = bwd_flop * steps / (t["bwd_ms"] * 1e-3) / 1e12
+        peak, src = choose_peak(peaks, t["clocks"])
+        res[key] = {
+            "workload": f"{w.key}: {w.title}", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "S": w.S,
+            "cp_size": w.cp_size, "L": w.L, "window": w.window, "kv": w.kv, "ranks": [s["r"] for s in rep.plan],
+            "pairs": sum(s["pairs"] for s in rep.shards), "value": round(value, 2), "unit": UNIT,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 4),
+            "tokens_per_s": round(w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
+            "fwd_tflops": round(fwd_flop * steps / (t["fwd_ms"] * 1e-3) / 1e12, 2),
+            "bwd_main_tflops": round(bwd_tf, 2), "peak": peak, "peak_source": src,
+            "frac": round(value / peak, 4),
+            "frac_of_burst": round(value / peaks["bf16_tflops"], 4) if peaks.get("bf16_tflops") else None,
+            "frac_of_sustained": (round(value / peaks["bf16_tflops_sustained"], 4)
+                                  if peaks.get("bf16_tflops_sustained") else None),
+            "gpu_launches": rep.launches_per_step * steps, "clocks": t["clocks"],
+        }
+        del rep
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -527,43 +627,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         rep = Replica(w, rank_seed(args.seed, rank), dev, grad_dtype, ranks, deterministic=args.deterministic,
                       fwd_only=args.fwd_only)
     total_flop, fwd_flop, bwd_flop = rep.flops()
-
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
-
-    for _ in range(args.warmup):
-        rep.step()
-    torch.cuda.synchronize()
-    if int(rep.status.item()) != 0:
-        raise RuntimeError(f"device status {int(rep.status.item()):#x} after warm-up")
-
-    n = len(rep.shards)
-    ev_steps = [{"fwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
-                 "bwd": [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)],
-                 "merge": []}
-                for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
-    smi_index = visible[local_rank].strip() if local_rank < len(visible) else str(local_rank)
-    with ClockSampler(smi_index) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        start.record()
-        for k in range(args.steps):
-            rep.step(ev_steps[k])
-        stop.record()
-        torch.cuda.synchronize()
-        barrier()
-    clocks = clk.summary()
-    if int(rep.status.item()) != 0:
-        raise RuntimeError(f"device status {int(rep.status.item()):#x} in the timed region")
-    ms = start.elapsed_time(stop)
-    fwd_ms = sum(e["fwd"][i][0].elapsed_time(e["fwd"][i][1]) for e in ev_steps for i in range(n))
+    t = timed_steps(rep, args.steps, args.warmup, world, local_rank)
+    clocks = t["clocks"]
+    ms, fwd_ms, bwd_ms, merge_ms, n_merge = t["ms"], t["fwd_ms"], t["bwd_ms"], t["merge_ms"], t["n_merge"]
     fwd_only = getattr(rep, "fwd_only", False)
-    bwd_ms = 0.0 if fwd_only else sum(e["bwd"][i][0].elapsed_time(e["bwd"][i][1]) for e in ev_steps for i in range(n))
-    merge_ms = sum(a.elapsed_time(b) for e in ev_steps for a, b in e["merge"])
-    n_merge = sum(len(e["merge"]) for e in ev_steps)
     ms = allreduce_max(ms, dev, world)
     ms_per_step = ms / args.steps
 
@@ -576,7 +643,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     peaks = read_peaks()
     value = job_tflops(total_flop, ms_per_step, world)
     bwd_achieved = bwd_flop * args.steps / (bwd_ms * 1e-3) / 1e12 if bwd_ms > 0 else 0.0
-    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    peak, peak_source = choose_peak(peaks, clocks)
+    burst, sust = peaks.get("bf16_tflops"), peaks.get("bf16_tflops_sustained")
+    fracs = lambda a: {"frac_of_burst": round(a / burst, 4) if burst else None,
+                       "frac_of_sustained": round(a / sust, 4) if sust else None}
     traffic = None
     if (TRAFFIC["bytes_per_launch"] and TRAFFIC["source_sha256"] == kernel_source_sha() and not chunked
             and w.key == TRAFFIC["workload"] and not getattr(rep, "deterministic", False)):
@@ -598,6 +668,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                  + ("in the forward's epilogue" if rep.fused else "by the merge kernel"))
                                 if chunked else "none"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "peak": peak, "peak_source": peak_source, **fracs(value / world),
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
@@ -607,7 +678,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                 f"{BWD_KERNEL[w.D]} (backward main stage, with its dK/dV zero-fill launch)"),
                      "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
-                     "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
+                     **fracs(bwd_achieved), "peak_source": peak_source,
                      "traffic": traffic,
                      "flops_per_launch": bwd_flop / n_bwd,
                      "avg_launch_ms": round(bwd_ms / (args.steps * n_bwd), 4)},
@@ -622,8 +693,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["e2e_note"] = "forward only: the end-to-end timing covers the whole path"
         line["roofline"] = {"kernel": f"fwd{'512' if w.D == 512 else ''}_kernel (forward, D {w.D})", "bound": "tensor",
                             "achieved": round(fwd_achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                            "frac": round(fwd_achieved / peak, 4),
-                            "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a multi-second loop)",
+                            "frac": round(fwd_achieved / peak, 4), **fracs(fwd_achieved),
+                            "peak_source": peak_source,
                             "traffic": None, "flops_per_launch": fwd_flop / len(rep.shards),
                             "avg_launch_ms": round(fwd_s * 1e3, 4)}
         del line["bwd_main_tflops"]
@@ -638,6 +709,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_launch": rep.merge_bytes(),
                 "avg_launch_ms": round(merge_ms / n_merge, 4), "launches": n_merge,
                 "share_of_step": round(merge_ms / ms, 4)}
+    if world == 1 and args.configs and not chunked and not fwd_only and not getattr(rep, "deterministic", False):
+        del rep
+        torch.cuda.empty_cache()
+        line["configs"] = run_other_configs(args, dev, local_rank, peaks)
     return line
 
 
@@ -812,6 +887,9 @@ def main():
                     help="ring: each shard's K/V in per-rank chunks, each chunk's forward merged in its epilogue, "
                          "backward per chunk; ring-merge: the same with the separate merge kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--configs", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time C3, C4 (rank 15), C5w512 and G512 (a few steps each) into the line's "
+                         "'configs' block (single GPU, default workload path only)")
     ap.add_argument("--cpu-heads", type=int, default=None,
                     help="query heads of batch row 0 in the oracle's timed CPU-baseline slice "
                          "(default: about 10-30 s of CPU work; 8 for head dim 512, else 32)")

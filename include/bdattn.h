@@ -262,24 +262,32 @@ int bd_attn_bwd_main_dq(const void* dout, const void* q, const void* k, const vo
 
 /* Allocation-free backward. Same arguments and results as bd_attn_bwd
  * except that there is no `workspace`: the dq accumulator and delta live in
- * one scratch array that the library places in device memory at load time
- * (BD_NOALLOC_SCRATCH_BYTES per GPU, held until the process exits). It is for
- * callers that can hand the library their inputs and outputs but cannot
- * allocate device memory at call time -- for example a host that reserved
- * its whole memory budget up front, or a plugin whose framework forbids
- * allocations outside its own allocator -- so it calls no cudaMalloc,
- * cudaFree or allocating routine. The paper pages have no counterpart; this
- * is a deployment convenience.
+ * one static scratch array of BD_NOALLOC_SCRATCH_BYTES per GPU, part of the
+ * library's device code and held until the process exits. It is for callers
+ * that can hand the library their inputs and outputs but cannot allocate
+ * device memory at call time -- for example a host that reserved its whole
+ * memory budget up front, or a plugin whose framework forbids allocations
+ * outside its own allocator -- so it calls no cudaMalloc, cudaFree or
+ * allocating routine. The paper pages have no counterpart; this is a
+ * deployment convenience.
  *  - Returns BD_ERR_SCRATCH_TOO_SMALL (nothing enqueued) when
  *    bd_attn_bwd_workspace_bytes(g) exceeds BD_NOALLOC_SCRATCH_BYTES.
- *  - The first call on each device looks up the scratch array's device
- *    address (cudaGetSymbolAddress, with that device current); make that
- *    first call before any stream capture.
+ *  - Set-up: the first call on each device (with that device current) looks
+ *    up the array's device address (cudaGetSymbolAddress). Under CUDA's lazy
+ *    module loading (the default) that is also when the driver loads the
+ *    library's code holding the array and so takes its device memory; with
+ *    CUDA_MODULE_LOADING=EAGER it is taken when the context is created. A
+ *    caller that reserves its memory budget up front should therefore do the
+ *    set-up first: a call with every pointer argument NULL (g included) does
+ *    only the set-up of the current device, enqueues nothing and returns
+ *    BD_OK. Make the set-up before any stream capture. If the array cannot be
+ *    placed, the call returns BD_ERR_NOALLOC_SETUP.
  *  - Every call on a device shares the one array, and each call starts by
  *    zeroing the part it accumulates into. Calls whose kernels overlap on the
  *    GPU (other streams, other host threads) race on it: serialise them. */
 #define BD_NOALLOC_SCRATCH_BYTES (16u << 20)
 #define BD_ERR_SCRATCH_TOO_SMALL 4
+#define BD_ERR_NOALLOC_SETUP 5
 int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq, void* dk,
                         void* dv, int32_t* status, bd_stream_t stream);

@@ -450,8 +450,12 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
 
 // ------------------------------------------------- allocation-free backward
 // The backward's scratch (fp32 dq accumulator + delta) for callers that cannot
-// allocate device memory at call time: one array per GPU, reserved when the
-// library is loaded and shared by every bd_attn_bwd_noalloc call on that GPU.
+// allocate device memory at call time: one array per GPU, shared by every
+// bd_attn_bwd_noalloc call on that GPU and held until the process exits. The
+// CUDA driver places it in device memory when it loads this file's code on a
+// device: when the context is created under CUDA_MODULE_LOADING=EAGER, else
+// (lazy loading, the default) at the first use of this file's code there,
+// which is at the latest the set-up below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[BD_NOALLOC_SCRATCH_BYTES];
 
 namespace {
@@ -459,16 +463,20 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device. Looked up once
-// per device (with that device current); host code must never hand the
-// symbol itself to a kernel, it is only a host-side stand-in.
+// Set-up, once per device with that device current: the device address of
+// g_noalloc_scratch. Host code must never hand the symbol itself to a kernel;
+// on the host it is only a stand-in. A failure here (typically the driver
+// finding no room to load the array) is reported as BD_ERR_NOALLOC_SETUP.
 int noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // clear the (non-sticky) error so that later launches do not report it
+      return BD_ERR_NOALLOC_SETUP;
+    }
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -481,6 +489,12 @@ extern "C" {
 int bd_attn_bwd_noalloc(const void* dout, const void* q, const void* k, const void* v, const void* out,
                         const float* lse, const void* seg, const bd_geom* gi, int grad_dtype, void* dq, void* dk,
                         void* dv, int32_t* status, bd_stream_t stream) {
+  // every pointer NULL: only the set-up of the current device, nothing enqueued
+  if (!dout && !q && !k && !v && !out && !lse && !seg && !gi && !dq && !dk && !dv && !status) {
+    if (int rc = check_device()) return rc;
+    void* scratch = nullptr;
+    return noalloc_scratch(&scratch);
+  }
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
   if (bwd_workspace_bytes(g) > BD_NOALLOC_SCRATCH_BYTES) return BD_ERR_SCRATCH_TOO_SMALL;
@@ -499,6 +513,10 @@ const char* bd_attn_strerror(int code) {
     case BD_ERR_UNSUPPORTED: return "device is not a Blackwell sm_10x GPU";
     case BD_ERR_SCRATCH_TOO_SMALL:
       return "problem needs more backward scratch than bd_attn_bwd_noalloc's static 16 MiB (use bd_attn_bwd)";
+    case BD_ERR_NOALLOC_SETUP:
+      return "bd_attn_bwd_noalloc could not place its static 16 MiB scratch on this device (no free device memory "
+             "when the library's code was loaded: do the set-up call before reserving memory, or run with "
+             "CUDA_MODULE_LOADING=EAGER)";
     default: return "unknown bdattn error code";
   }
 }

@@ -95,3 +95,26 @@ def real_rows(c: dict) -> np.ndarray:
     ro = c["row_offset"]
     r = c["doc"][:, ro:ro + w.L] != 0
     return np.repeat(r[:, None, :], w.Hq, axis=1)
+
+
+# bf16 gradients: the fp32 result rounded once to bf16 (relative error <= 2^-8,
+# half a unit in the last of bf16's 8 significant bits) on top of the fp32
+# accumulation error the parity bar already covers
+BF16_REL = 2.0 ** -8
+
+
+def assert_close_bf16(name: str, got, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS, rel=BF16_REL):
+    """Element-wise |got - ref| <= max_abs + rel |ref|; mean-abs over the whole
+    tensor <= mean_abs + rel mean |ref|."""
+    got = got.detach().double().cpu().numpy() if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    d = np.abs(got - ref)
+    bound = max_abs + rel * np.abs(ref)
+    worst = int(np.argmax(d - bound)) if d.size else 0
+    assert (d <= bound).all(), (f"{name}: |err| {d.flat[worst]:.3e} > {bound.flat[worst]:.3e} "
+                                f"at {np.unravel_index(worst, d.shape)} (ref {ref.flat[worst]:.4f})")
+    if d.size:
+        assert d.mean() <= mean_abs + rel * np.abs(ref).mean(), f"{name}: mean-abs {d.mean():.3e}"
+    return float(d.max(initial=0.0)), float(d.mean()) if d.size else 0.0

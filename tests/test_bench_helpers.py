@@ -37,3 +37,18 @@ def test_headline_pair_count_is_stable():
     g = oracle.geom(w.B, 1, 1, 128, w.S, w.L, 3 * w.L, 0, w.S)
     assert plan[3]["pairs"] == oracle.pairs(doc, g)
     assert total > 0
+
+
+def test_peak_follows_the_clock_record():
+    """Burst peak when the timed region ran at the maximum SM clock with no power
+    cap; the sustained (power-capped) peak otherwise or when clocks are unknown."""
+    peaks = {"source": "measured", "bf16_tflops": 1891.6, "bf16_tflops_sustained": 1686.5}
+    p, src = bench.choose_peak(peaks, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert p == 1891.6 and "burst" in src
+    assert round(792.8 / p, 2) == 0.42
+    for clocks in ({"sm_mhz": 1432.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]},
+                   {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]},
+                   {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": []},
+                   {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}):
+        p, src = bench.choose_peak(peaks, clocks)
+        assert p == 1686.5 and "sustained" in src, clocks
