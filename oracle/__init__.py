@@ -15,7 +15,11 @@ What it computes follows the NeMo AutoModel API pages:
   * ``gemma4_moe.cp_local_ring`` (module text) -- bottom-right causal plus a
     left window for the sliding layer, read as ``p - s < window``; the
     per-chunk forward over a part of the keys and the ``-inf``-safe online
-    softmax merge of chunk results (``fwd_chunk``, ``merge``).
+    softmax merge of chunk results (``fwd_chunk``, ``merge``);
+  * ``blockdiag_cp.kernels._cp_blockdiag_varlen(..., dropout_p)`` -- attention
+    dropout, read as inverted dropout on the attention probabilities with the
+    keep decisions drawn by Philox-4x32-10 (Salmon et al., SC'11) from a
+    counter of (key position / 8, query position, query head, batch row).
 
 Every attention function here is a plain loop in ``bdattn_oracle.c`` (fp64,
 OpenMP over independent rows); ``merge`` is its formula written out in numpy.
@@ -54,7 +58,8 @@ class Geom(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
                 ("S_full", ctypes.c_int), ("L", ctypes.c_int), ("row_offset", ctypes.c_int),
                 ("kv_offset", ctypes.c_int), ("S_kv", ctypes.c_int), ("window", ctypes.c_int),
-                ("scale", ctypes.c_double)]
+                ("scale", ctypes.c_double), ("dropout_p", ctypes.c_double), ("seed_lo", ctypes.c_uint32),
+                ("seed_hi", ctypes.c_uint32)]
 
 
 def _load():
@@ -78,15 +83,42 @@ def _load():
             lib.og_fwd_rows_chunk.restype = ctypes.c_int
             lib.og_bwd.argtypes = [P, P, P, P, P, G, P, ctypes.c_int, P, ctypes.c_int, P, P, P]
             lib.og_bwd.restype = ctypes.c_int
+            lib.og_philox.argtypes = [P, P, ctypes.c_int, P]
+            lib.og_philox.restype = ctypes.c_int
+            lib.og_dropout_factors.argtypes = [G, ctypes.c_int, ctypes.c_int, P]
+            lib.og_dropout_factors.restype = ctypes.c_int
             _lib = lib
     return _lib
 
 
-def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=None) -> Geom:
+def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=None, dropout_p=0.0,
+         seed=0) -> Geom:
+    """Geometry of one shard; dropout_p > 0 turns on attention dropout drawn
+    from the 64-bit `seed` (Philox key = low, high 32 bits)."""
     if scale is None or scale <= 0:
         scale = float(D) ** -0.5
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
     return Geom(int(B), int(Hq), int(Hkv), int(D), int(S_full), int(L), int(row_offset), int(kv_offset),
-                int(S_kv), int(window), float(scale))
+                int(S_kv), int(window), float(scale), float(dropout_p), seed & 0xFFFFFFFF, seed >> 32)
+
+
+def philox(ctr, key) -> np.ndarray:
+    """Philox-4x32-10 (Salmon et al., SC'11): ctr [n, 4], key [n, 2] uint32 ->
+    [n, 4] uint32, one independent evaluation per row."""
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32).reshape(-1, 4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(-1, 2))
+    assert c.shape[0] == k.shape[0]
+    out = np.zeros_like(c)
+    _check(_load().og_philox(_ptr(c), _ptr(k), c.shape[0], _ptr(out)), "philox")
+    return out
+
+
+def dropout_factors(g: Geom, b: int, h: int) -> np.ndarray:
+    """[L, S_kv] dropout factor of every (local row, K/V buffer row) pair of batch
+    row b, query head h: 0 (dropped) or the keep scale; all 1 without dropout."""
+    z = np.zeros((g.L, g.S_kv), dtype=np.float64)
+    _check(_load().og_dropout_factors(ctypes.byref(g), int(b), int(h), _ptr(z)), "dropout_factors")
+    return z
 
 
 def _f64(x) -> np.ndarray:

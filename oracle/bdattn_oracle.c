@@ -24,6 +24,16 @@
  *              bottom-right causal attention with a left window.
  *  [A.lse]     gemma4_moe.cp_attention, `_scatter_lse`: LSE is -inf on rows
  *              that take no part.
+ *  [K.drop]    blockdiag_cp.kernels, `_cp_blockdiag_varlen`, argument
+ *              `dropout_p` (attention dropout probability); the same argument
+ *              on the FlashAttention varlen helpers and ring-attention
+ *              functions of gemma4_moe.cp_attention. Read as inverted
+ *              dropout on the attention probabilities: each allowed P_ps is
+ *              kept with probability 1 - p and scaled by the inverse of that
+ *              probability, the LSE stays that of the undropped softmax.
+ *  [Philox]    J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
+ *              random numbers: as easy as 1, 2, 3", SC'11: the counter-based
+ *              generator Philox-4x32-10 that draws the keep decisions.
  *
  * The window is read as p - s < W (W <= 0: no window). The LSE is the natural
  * logarithm. GQA maps query head h to kv head h / (Hq / Hkv).
@@ -45,6 +55,8 @@ typedef struct {
   int S_kv;       /* K/V buffer rows */
   int window;     /* <= 0: none */
   double scale;
+  double dropout_p;            /* [K.drop] probability of dropping an attention weight; 0: none */
+  uint32_t seed_lo, seed_hi;   /* [Philox] key of the dropout stream */
 } og_geom;
 
 /* Error codes returned by the oracle entry points. */
@@ -62,8 +74,80 @@ static int og_allowed(const int32_t* doc_row, int p, int s, int window) {
   return 1;
 }
 
+/* ------------------------------------------------------------- dropout --- */
+
+/* [Philox] Philox-4x32 with R = 10 rounds. The state is four 32-bit words
+ * (the counter) and the key two 32-bit words. One round multiplies words 0
+ * and 2 by the round multipliers M0 = 0xD2511F53 and M1 = 0xCD9E8D57 (full
+ * 64-bit products) and forms the new state
+ *   ( hi(M1 x2) ^ x1 ^ k0,  lo(M1 x2),  hi(M0 x0) ^ x3 ^ k1,  lo(M0 x0) );
+ * between rounds the key is bumped by the Weyl constants W0 = 0x9E3779B9
+ * (golden ratio) and W1 = 0xBB67AE85 (sqrt(3) - 1). The first round uses the
+ * key as given. */
+static void og_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * x0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * x2;
+    const uint32_t y0 = (uint32_t)(p1 >> 32) ^ x1 ^ k0;
+    const uint32_t y1 = (uint32_t)p1;
+    const uint32_t y2 = (uint32_t)(p0 >> 32) ^ x3 ^ k1;
+    const uint32_t y3 = (uint32_t)p0;
+    x0 = y0;
+    x1 = y1;
+    x2 = y2;
+    x3 = y3;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+/* Test hook: n independent evaluations, ctr[n][4], key[n][2] -> out[n][4]. */
+int og_philox(const uint32_t* ctr, const uint32_t* key, int n, uint32_t* out) {
+  if (n < 0 || (n > 0 && (!ctr || !key || !out))) return OG_ERR_ARG;
+  for (int i = 0; i < n; ++i) og_philox4x32_10(ctr + 4 * i, key + 2 * i, out + 4 * i);
+  return OG_OK;
+}
+
+/* Keep threshold on a 16-bit uniform: T = round(p * 2^16). A weight is kept
+ * iff its 16-bit draw u >= T, i.e. with probability (2^16 - T) / 2^16. */
+static uint32_t og_drop_threshold(double p) { return (uint32_t)floor(p * 65536.0 + 0.5); }
+
+/* Scale of a kept weight: the inverse of the keep probability. */
+static double og_drop_scale(const og_geom* g) {
+  const uint32_t T = og_drop_threshold(g->dropout_p);
+  return 65536.0 / (double)(65536u - T);
+}
+
+/* The 16-bit draw of the pair (query head h, query position p, key position s)
+ * of batch row b: one Philox call covers eight consecutive key positions of
+ * one query row; counter = (s / 8, p, h, b), key = (seed_lo, seed_hi); key s
+ * takes the 16-bit piece s mod 8 of the 128-bit output (word (s mod 8) / 2,
+ * low half for even s, high half for odd s). Positions are global. */
+static uint32_t og_drop_u16(const og_geom* g, int b, int h, int p, int s) {
+  const uint32_t ctr[4] = {(uint32_t)s >> 3, (uint32_t)p, (uint32_t)h, (uint32_t)b};
+  const uint32_t key[2] = {g->seed_lo, g->seed_hi};
+  uint32_t r[4];
+  og_philox4x32_10(ctr, key, r);
+  const uint32_t w = r[(s & 7) >> 1];
+  return (s & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+/* Multiplier of P_ps in the output: 0 (dropped), the keep scale (kept), or 1
+ * without dropout. */
+static double og_drop_factor(const og_geom* g, int b, int h, int p, int s) {
+  if (g->dropout_p <= 0.0) return 1.0;
+  return og_drop_u16(g, b, h, p, s) >= og_drop_threshold(g->dropout_p) ? og_drop_scale(g) : 0.0;
+}
+
 static int og_geom_ok(const og_geom* g) {
   if (!g || g->B <= 0 || g->Hq <= 0 || g->Hkv <= 0 || g->D <= 0) return 0;
+  if (!(g->dropout_p >= 0.0 && g->dropout_p < 1.0) || og_drop_threshold(g->dropout_p) > 65535u) return 0;
   if (g->Hq % g->Hkv) return 0;
   if (g->L < 0 || g->S_kv < 0 || g->S_full <= 0) return 0;
   if (g->row_offset < 0 || g->row_offset + g->L > g->S_full) return 0;
@@ -245,9 +329,10 @@ static int og_fwd_row(const double* q, const double* k, const double* v, const i
   for (int j = 0; j < g->S_kv; ++j) {
     if (xbuf[j] == -INFINITY) continue;
     const double w = exp(xbuf[j] - m);
-    l += w;
+    l += w;  /* [K.drop] the softmax normaliser is the undropped one */
+    const double wz = w * og_drop_factor(g, b, h, p, g->kv_offset + j);
     const double* vr = vb + (size_t)j * D;
-    for (int d = 0; d < D; ++d) out_row[d] += w * vr[d];
+    for (int d = 0; d < D; ++d) out_row[d] += wz * vr[d];
   }
   for (int d = 0; d < D; ++d) out_row[d] /= l;
   *lse_out = m + log(l);
@@ -335,10 +420,11 @@ int og_fwd_rows_chunk(const double* q, const double* k, const double* v, const i
  * (dq) and selected keys (dk, dv summed over the query heads of the key's
  * GQA group):
  *   P_ps  = exp(scale q_p.k_s - lse_p)         (allowed pairs, real rows)
- *   delta = dout_p . out_p
- *   dS_ps = P_ps (dout_p . v_s - delta_p)
+ *   Z_ps  = dropout factor (0 or the keep scale; 1 without dropout)
+ *   delta = dout_p . out_p                      (out = sum_s P Z v)
+ *   dS_ps = P_ps (Z_ps dout_p . v_s - delta_p)
  *   dq_p  = scale sum_s dS_ps k_s
- *   dk_s  = scale sum_p dS_ps q_p ,  dv_s = sum_p P_ps dout_p
+ *   dk_s  = scale sum_p dS_ps q_p ,  dv_s = sum_p P_ps Z_ps dout_p
  * Padding query rows contribute nothing and get dq = 0 ([K.varlen]).
  *
  * rows[nr][3] = (b, h, i) -> dq[nr][D]
@@ -433,7 +519,8 @@ int og_bwd(const double* q, const double* k, const double* v, const double* dout
       if (!og_allowed(row, p, g->kv_offset + j, g->window)) continue;
       const double* kr = kb + (size_t)j * D;
       const double P = exp(g->scale * og_dot(qr, kr, D) - lse_all[r]);
-      const double dS = P * (og_dot(dor, vb + (size_t)j * D, D) - delta_all[r]);
+      const double Z = og_drop_factor(g, b, h, p, g->kv_offset + j);
+      const double dS = P * (Z * og_dot(dor, vb + (size_t)j * D, D) - delta_all[r]);
       for (int d = 0; d < D; ++d) dqr[d] += g->scale * dS * kr[d];
     }
   }
@@ -458,9 +545,10 @@ int og_bwd(const double* q, const double* k, const double* v, const double* dout
         const double* qr = q + r * D;
         const double* dor = dout + r * D;
         const double P = exp(g->scale * og_dot(qr, kr, D) - lse_all[r]);
-        const double dS = P * (og_dot(dor, vr, D) - delta_all[r]);
+        const double Z = og_drop_factor(g, b, h, p, s);
+        const double dS = P * (Z * og_dot(dor, vr, D) - delta_all[r]);
         for (int d = 0; d < D; ++d) {
-          dvr[d] += P * dor[d];
+          dvr[d] += P * Z * dor[d];
           dkr[d] += g->scale * dS * qr[d];
         }
       }
@@ -472,4 +560,16 @@ done:
   free(lse_all);
   free(delta_all);
   return err;
+}
+
+/* Test hook: the dropout factor Z of every (local row i, K/V buffer row j) for
+ * batch row b and query head h, [L][S_kv], whether or not the pair is allowed
+ * (1 everywhere without dropout). */
+int og_dropout_factors(const og_geom* g, int b, int h, double* z) {
+  if (!og_geom_ok(g) || !z || b < 0 || b >= g->B || h < 0 || h >= g->Hq) return OG_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int i = 0; i < g->L; ++i)
+    for (int j = 0; j < g->S_kv; ++j)
+      z[(size_t)i * g->S_kv + j] = og_drop_factor(g, b, h, g->row_offset + i, g->kv_offset + j);
+  return OG_OK;
 }
