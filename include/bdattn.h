@@ -70,7 +70,26 @@ typedef struct {
   int window;     /* left window W (> 0: also require p - s < W); <= 0: none */
   float scale;    /* softmax scale; <= 0 means D^-0.5 */
   int kv_layout;  /* layout of k, v, dk, dv: BD_KV_BHSD (0) or BD_KV_SBHD (1) */
+  float dropout_p;  /* attention dropout probability, 0 <= p < 1 (0: none); see below */
+  uint32_t seed_lo; /* dropout seed: low and high 32 bits (the Philox key) */
+  uint32_t seed_hi;
 } bd_geom;
+
+/* Attention dropout (blockdiag_cp.kernels, `_cp_blockdiag_varlen` argument
+ * `dropout_p`: attention dropout probability). Inverted dropout on the
+ * softmax probabilities: out_p = sum_s P_ps Z_ps v_s with Z_ps = 0 (dropped)
+ * or 2^16 / (2^16 - T) (kept); the LSE is that of the undropped softmax, and
+ * the backward takes the same Z (dV = sum_p P Z dO, dS = P (Z dP - delta)).
+ * The decision of the pair (query head h, global query position p, global key
+ * position s) of batch row b: Philox-4x32-10 (Salmon et al., SC'11) with
+ * counter (s / 8, p, h, b) and key (seed_lo, seed_hi) gives eight 16-bit draws,
+ * key s taking draw s mod 8 (word (s mod 8) / 2; low half for even s); the pair
+ * is kept iff its draw u >= T = round(dropout_p * 2^16). Decisions depend on
+ * global positions only, so K/V chunks, shards and buffer offsets agree.
+ * Dropout is built for D = 64, 128 and 256: every forward and backward entry
+ * point returns BD_ERR_ARG for dropout_p > 0 at D = 512, and for dropout_p
+ * outside [0, 1) or rounding to T = 2^16. A forward and the backward of the
+ * same step must use the same dropout_p and seed. */
 
 /* K/V layouts. BD_KV_SBHD is token-major, [S_kv][B][Hkv][D]: the receive
  * buffer of the needed-only all-to-all-v (pieces in source order make the

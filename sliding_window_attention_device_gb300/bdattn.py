@@ -52,7 +52,8 @@ class Geom(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("D", ctypes.c_int),
                 ("S_full", ctypes.c_int), ("L", ctypes.c_int), ("row_offset", ctypes.c_int),
                 ("kv_offset", ctypes.c_int), ("S_kv", ctypes.c_int), ("window", ctypes.c_int),
-                ("scale", ctypes.c_float), ("kv_layout", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("kv_layout", ctypes.c_int), ("dropout_p", ctypes.c_float),
+                ("seed_lo", ctypes.c_uint32), ("seed_hi", ctypes.c_uint32)]
 
     def __repr__(self):
         return "Geom(" + ", ".join(f"{n}={getattr(self, n)}" for n, _ in self._fields_) + ")"
@@ -61,13 +62,18 @@ class Geom(ctypes.Structure):
 KV_BHSD, KV_SBHD = 0, 1  # K/V layouts: [B, Hkv, S_kv, D] or token-major [S_kv, B, Hkv, D]
 
 
-def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=0.0, kv_layout=KV_BHSD) -> Geom:
+def geom(B, Hq, Hkv, D, S_full, L, row_offset, kv_offset, S_kv, window=0, scale=0.0, kv_layout=KV_BHSD,
+         dropout_p=0.0, seed=0) -> Geom:
     """Geometry of one query shard: local rows [row_offset, row_offset+L) of a
     padded sequence of S_full positions, K/V buffer rows = positions
     [kv_offset, kv_offset+S_kv). scale <= 0 means D**-0.5; window <= 0: none;
-    kv_layout: KV_BHSD or KV_SBHD (token-major k, v, dk, dv)."""
+    kv_layout: KV_BHSD or KV_SBHD (token-major k, v, dk, dv); dropout_p > 0:
+    attention dropout drawn from the 64-bit `seed` (the same p and seed in the
+    forward and the backward of a step)."""
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
     return Geom(int(B), int(Hq), int(Hkv), int(D), int(S_full), int(L), int(row_offset), int(kv_offset),
-                int(S_kv), int(window), float(scale or 0.0), int(kv_layout))
+                int(S_kv), int(window), float(scale or 0.0), int(kv_layout), float(dropout_p), seed & 0xFFFFFFFF,
+                seed >> 32)
 
 
 def kv_shape(g: Geom) -> tuple:

@@ -18,10 +18,15 @@
 //   warps 4-7 and 12-15 P and dS (thread = key row, q columns 0-63 / 64-127);
 //   warps 8-11 read dQ^T (thread = d row) and add it to the fp32 accumulator
 //   with red.global.add (128-byte coalesced per warp instruction).
+// With attention dropout (kDrop) each P / dS warp draws its 32 keys' keep
+// masks over the tile's q columns before S arrives; the dropped weights are
+// zeroed in P^T (the dV operand), dS = P (Z dP - delta) takes the same
+// decisions, and dV is scaled by the keep scale when it is written.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -78,7 +83,7 @@ __host__ __device__ constexpr size_t bwd128_smem_bytes() {
 
 // kDq: also the dq products and their reductions (else dK / dV only, for a
 // separate deterministic dq pass)
-template <int D, bool kDq>
+template <int D, bool kDq, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -359,12 +364,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     const int row_end = min(doc_end, g.window > 0 ? key + g.window : 0x3fffffff);
+    // dropout: scale * keep scale multiplies a kept dP (a dropped one is zero)
+    const float sc_dp = kDrop ? g.scale * g.drop_scale : g.scale;
     bool ok = true;
-    int qt = 0;
+    int qt = 0, gq = 0;
     for (int it = 0; it < n_it; ++it) {
       const int st = it & 1;
       const int q0 = (q_lo + qt) * kQ;
-      if (++qt == nq) qt = 0;
+      uint64_t km = 0;  // dropout: keep bits of this key over the half's 64 q columns
+      if constexpr (kDrop)
+        km = key_keep_mask<8>(g, b, hk * G + gq, g.row_offset + q0 + c0, g.kv_offset + kt * kTile + (warp & 3) * 32,
+                              lane);
+      if (++qt == nq) {
+        qt = 0;
+        ++gq;
+      }
       if (!warp_wait(&s.q_full[st], (it >> 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       if (!warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       tc_fence_after();
@@ -393,7 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed bf16 P of these 32 q columns over S^T columns this half has read
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[32 * h2 + 2 * e], p[32 * h2 + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) {
+          const int c = 32 * h2 + 2 * e;
+          if constexpr (kDrop)
+            pk[e] = pack_bf16x2(((km >> c) & 1u) ? p[c] : 0.f, ((km >> (c + 1)) & 1u) ? p[c + 1] : 0.f);
+          else
+            pk[e] = pack_bf16x2(p[c], p[c + 1]);
+        }
         tmem_st16(tbase + lane_off + kColS + c0 + 16 * h2, pk);
       }
       tmem_wait_st();
@@ -415,10 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 4; ++c4) {
           const float4 dl = d4[c4];
           const int c = 16 * h4 + 4 * c4;
-          dsk[2 * c4] = pack_bf16x2(p[c] * fmaf(__uint_as_float(sr[4 * c4]), g.scale, -dl.x),
-                                    p[c + 1] * fmaf(__uint_as_float(sr[4 * c4 + 1]), g.scale, -dl.y));
-          dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(__uint_as_float(sr[4 * c4 + 2]), g.scale, -dl.z),
-                                        p[c + 3] * fmaf(__uint_as_float(sr[4 * c4 + 3]), g.scale, -dl.w));
+          float dp[4] = {__uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1]), __uint_as_float(sr[4 * c4 + 2]),
+                         __uint_as_float(sr[4 * c4 + 3])};
+          if constexpr (kDrop) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dp[e] = ((km >> (c + e)) & 1u) ? dp[e] : 0.f;
+          }
+          dsk[2 * c4] = pack_bf16x2(p[c] * fmaf(dp[0], sc_dp, -dl.x), p[c + 1] * fmaf(dp[1], sc_dp, -dl.y));
+          dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(dp[2], sc_dp, -dl.z), p[c + 3] * fmaf(dp[3], sc_dp, -dl.w));
         }
         // 32 B of this key row of dS^T (128B-swizzled K-major layout)
 #pragma unroll
@@ -445,8 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + lane_off + kColDv + c, vv);
           tmem_wait_ld();
           if (j < g.S_kv) {
+            const float dvs = kDrop ? g.drop_scale : 1.0f;  // dropout: the keep scale of P^T
 #pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * dvs;
             store_row(dv, kv_row(g, b, hk, j) * D + c, f);
           }
           tmem_ld32(tbase + lane_off + kColDk + c, vv);
@@ -536,7 +561,9 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   if (e != cudaSuccess) return e;
   const size_t smem = need + 1024 <= static_cast<size_t>(max_optin) ? need + 1024 : static_cast<size_t>(max_optin);
   if (smem < need) return cudaErrorInvalidValue;
-  auto kern = dq_acc ? bwd128_kernel<D, true> : bwd128_kernel<D, false>;  // no accumulator: dK / dV only
+  // no accumulator: dK / dV only
+  auto kern = g.drop_t ? (dq_acc ? bwd128_kernel<D, true, true> : bwd128_kernel<D, false, true>)
+                       : (dq_acc ? bwd128_kernel<D, true, false> : bwd128_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // only tiles some local row can reach by position get a working CTA; with

@@ -27,10 +27,14 @@
 //   warp 1  issues the MMAs          warp 2  owns the tensor memory
 //   warps 4-7 and 12-15  P, dS (thread = key row; q columns 0-31 / 32-63)
 //   warps 8-11  dQ read-out (thread = d row)
+// With attention dropout (kDrop) each P / dS warp draws its 32 keys' keep
+// masks over the half's q columns (dropout.cuh); dropped weights are zeroed in
+// P^T, dS = P (Z dP - delta), and dV is scaled by the keep scale when written.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -164,7 +168,7 @@ constexpr int kBwdModeIdle = 0;  // past the attended tiles (zeroed by the zero-
 constexpr int kBwdModeWork = 1;  // an attended K/V tile
 
 // kDq: with the dq products (else dK / dV only, for the fixed-order dq pass).
-template <int D, bool kDq>
+template <int D, bool kDq, bool kDrop>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -483,11 +487,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     const int win_end = g.window > 0 ? key + g.window : 0x3fffffff;
     const int row_end = min(doc_end, win_end);  // rows [key, row_end) attend this key
+    // dropout: scale * keep scale multiplies a kept dP (a dropped one is zero)
+    const float sc_dp = kDrop ? g.scale * g.drop_scale : g.scale;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it & 1;  // slot of this tile's row values
       int pass, h, q0;
       decode(it, pass, h, q0);
+      uint64_t km = 0;  // dropout: keep bits of this key over the half's 32 q columns
+      if constexpr (kDrop)
+        km = key_keep_mask<4>(g, b, h, g.row_offset + q0 + c0, g.kv_offset + kt * kTile + (warp & 3) * 32, lane);
       // the early group's copy also publishes this tile's row values
       const int ge = it > 0 ? 1 - (it - 1) / n_it_pass : 0;
       if (!warp_wait(&s.grp_full[ge], it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
@@ -515,7 +524,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      for (int c = 0; c < 16; ++c) {
+        if constexpr (kDrop)
+          pk[c] = pack_bf16x2(((km >> (2 * c)) & 1u) ? p[2 * c] : 0.f, ((km >> (2 * c + 1)) & 1u) ? p[2 * c + 1] : 0.f);
+        else
+          pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      }
       tmem_st16(tbase + lane_off + Cfg::kColS + 48 * half, pk);
       tmem_wait_st();
       tc_fence_before();
@@ -530,9 +544,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 dl = d4[c4];
         const int c = 4 * c4;
-        pk[2 * c4] = pack_bf16x2(p[c] * fmaf(__uint_as_float(sr[c]), g.scale, -dl.x), p[c + 1] * fmaf(__uint_as_float(sr[c + 1]), g.scale, -dl.y));
-        pk[2 * c4 + 1] =
-            pack_bf16x2(p[c + 2] * fmaf(__uint_as_float(sr[c + 2]), g.scale, -dl.z), p[c + 3] * fmaf(__uint_as_float(sr[c + 3]), g.scale, -dl.w));
+        float dp[4] = {__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), __uint_as_float(sr[c + 2]),
+                       __uint_as_float(sr[c + 3])};
+        if constexpr (kDrop) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dp[e] = ((km >> (c + e)) & 1u) ? dp[e] : 0.f;
+        }
+        pk[2 * c4] = pack_bf16x2(p[c] * fmaf(dp[0], sc_dp, -dl.x), p[c + 1] * fmaf(dp[1], sc_dp, -dl.y));
+        pk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(dp[2], sc_dp, -dl.z), p[c + 3] * fmaf(dp[3], sc_dp, -dl.w));
       }
       if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       // this half's 64 B of the key row of dS^T, 128B-swizzled K-major layout
@@ -557,8 +576,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(tbase + lane_off + Cfg::kColDv + c, vv);
           tmem_wait_ld();
           if (j < g.S_kv) {
+            const float dvs = kDrop ? g.drop_scale : 1.0f;  // dropout: the keep scale of P^T
 #pragma unroll
-            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * dvs;
             store_row(dv, kv_row(g, b, hk, j) * D + pass * kDp + c, f);
           }
           tmem_ld32(tbase + lane_off + Cfg::kColDk + c, vv);
@@ -687,7 +707,7 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
                           const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
                           cudaStream_t st) {
   const size_t smem = sizeof(BwdSmem<D, BwdCfg<D>::kNsq>) + 1024;  // + 1 KB to align the swizzled tiles
-  auto kern = bwd_kernel<D, kDq>;
+  auto kern = g.drop_t ? bwd_kernel<D, kDq, true> : bwd_kernel<D, kDq, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // only tiles some local row can reach by position get a working CTA; with

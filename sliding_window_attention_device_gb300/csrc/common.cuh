@@ -18,6 +18,9 @@ struct Geom {
   int S_full, L, row_offset, kv_offset, S_kv, window;
   float scale;
   int kv_tm;                      // k, v, dk, dv token-major: [S_kv][B][Hkv][D]
+  uint32_t drop_t;                // dropout: keep iff a pair's 16-bit draw >= drop_t; 0: no dropout
+  float drop_scale;               // dropout: factor of a kept weight, 2^16 / (2^16 - drop_t)
+  uint32_t seed_lo, seed_hi;      // dropout: Philox key
   int nqt, nkt, nkw;              // 128-row q tiles, 128-row K/V tiles, bitmap words per q tile
   int off[BD_SEG_NOFF];           // word offsets of the table regions
 };

@@ -20,6 +20,7 @@
 #include <cstdint>
 
 #include "dq_stream.cuh"
+#include "dropout.cuh"
 
 namespace bd {
 
@@ -48,6 +49,7 @@ struct Dq256Smem {
 };
 static_assert(sizeof(Dq256Smem) + 1024 <= 232448, "shared memory per CTA");
 
+template <bool kDrop>
 __global__ void __launch_bounds__(kThreads256, 1)
     bwd_dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -241,6 +243,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
     }
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
+      uint32_t km[4] = {0u, 0u, 0u, 0u};  // dropout: keep bits of this row over the tile's 128 keys
+      if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
       if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, vstatus)) {
         ok = false;
         break;
@@ -251,8 +255,8 @@ __global__ void __launch_bounds__(kThreads256, 1)
       const bool dead = !real || jhi < c0 || jlo > c0 + kTile - 1;
       const bool full = jlo <= c0 && c0 + kTile - 1 <= jhi;
       uint32_t pk[2][32];  // dS of keys [64 hf, 64 hf + 64), bf16 pairs
-      dq_form_ds(tbase + lane_off + kColS, tbase + lane_off + kColDp, g.scale, nl2, ndl, dead, full, jlo - c0,
-                 jhi - c0, pk);
+      dq_form_ds<kDrop>(tbase + lane_off + kColS, tbase + lane_off + kColDp, g.scale, nl2, ndl, dead, full, jlo - c0,
+                        jhi - c0, pk, km, g.drop_scale);
       // dS over this row's S columns (read above): the A operand of the dQ products
       tmem_st32(tbase + lane_off + kColS, pk[0]);
       tmem_st32(tbase + lane_off + kColS + 32, pk[1]);
@@ -293,11 +297,12 @@ cudaError_t launch_bwd_dq256(const CUtensorMap& mq, const CUtensorMap& mdo, cons
   e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(bwd_dq256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kern = g.drop_t ? bwd_dq256_kernel<true> : bwd_dq256_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * g.Hq;  // (q tile, query head)
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (const cudaError_t le = launch_pdl(bwd_dq256_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads256), smem,
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads256), smem,
       st, mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }

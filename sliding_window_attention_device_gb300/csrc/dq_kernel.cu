@@ -15,10 +15,13 @@
 //   warps 4-7  thread = q row: P, dS, and the dq rows at the end
 // D = 64 or 128 (S, dP and dQ fill 384 of the 512 tensor-memory columns);
 // D = 256 and 512 stream K/V through a chunk ring (dq256_kernel.cu, dq512_kernel.cu).
+// With attention dropout (kDrop) each row draws its keep mask of a K/V tile
+// (dropout.cuh) before the tile's S and dP arrive: dS = P (Z dP - delta).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -50,7 +53,7 @@ struct DqSmem {
 constexpr uint32_t kColS = 0, kColDp = 128, kColDq = 256;
 constexpr int kDqThreads = 256;
 
-template <int D, int NS>
+template <int D, int NS, bool kDrop>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -242,9 +245,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       ndl = delta[row0 + i] * -g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
     }
     const float2 sl2 = make_float2(g.scale * 1.4426950408889634f, g.scale * 1.4426950408889634f);
-    const float2 sc = make_float2(g.scale, g.scale), nl2v = make_float2(nl2, nl2), ndlv = make_float2(ndl, ndl);
+    const float scd = kDrop ? g.scale * g.drop_scale : g.scale;  // dropout: a kept dP's factor
+    const float2 sc = make_float2(scd, scd), nl2v = make_float2(nl2, nl2), ndlv = make_float2(ndl, ndl);
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
+      uint32_t km[4];  // dropout: keep bits of this row over the tile's 128 keys
+      if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
       if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, vstatus)) {
         ok = false;
         break;
@@ -282,7 +288,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             p0 = (c >= a_lo && c <= e_hi) ? p0 : 0.f;
             p1 = (c + 1 >= a_lo && c + 1 <= e_hi) ? p1 : 0.f;
           }
-          const float2 d = __ffma2_rn(make_float2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), sc, ndlv);
+          float dp0 = __uint_as_float(dr[2 * e]), dp1 = __uint_as_float(dr[2 * e + 1]);
+          if constexpr (kDrop) {
+            const uint32_t kb = km[c >> 5] >> (c & 31);
+            dp0 = (kb & 1u) ? dp0 : 0.f;
+            dp1 = (kb & 2u) ? dp1 : 0.f;
+          }
+          const float2 d = __ffma2_rn(make_float2(dp0, dp1), sc, ndlv);
           const float2 ds = __fmul2_rn(make_float2(p0, p1), d);
           pk[hf][e] = pack_bf16x2(ds.x, ds.y);
         }
@@ -354,7 +366,7 @@ cudaError_t launch_dq(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
-  auto kern = bwd_dq_kernel<D, NS>;
+  auto kern = g.drop_t ? bwd_dq_kernel<D, NS, true> : bwd_dq_kernel<D, NS, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * g.Hq;  // (q tile, query head)

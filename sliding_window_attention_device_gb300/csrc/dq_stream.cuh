@@ -16,11 +16,15 @@ namespace bd {
 //   dS = P (scale dP - scale delta),
 // as bf16 pairs (keys 2e, 2e + 1 of half hf in pk[hf][e]). t_s / t_dp: the
 // row's S and dP columns in tensor memory (128 each); nl2 = -lse log2(e),
-// ndl = -scale delta.
+// ndl = -scale delta. With attention dropout (kDrop), key c's dP counts only
+// when bit c of km is set and is scaled by drop_scale: dS = P (Z dP - delta).
+template <bool kDrop = false>
 __device__ __forceinline__ void dq_form_ds(uint32_t t_s, uint32_t t_dp, float scale, float nl2, float ndl,
-                                           bool dead, bool full, int a_lo, int e_hi, uint32_t (&pk)[2][32]) {
+                                           bool dead, bool full, int a_lo, int e_hi, uint32_t (&pk)[2][32],
+                                           const uint32_t (&km)[4] = {0u, 0u, 0u, 0u}, float drop_scale = 1.0f) {
   const float2 sl2 = make_float2(scale * 1.4426950408889634f, scale * 1.4426950408889634f);
-  const float2 sc = make_float2(scale, scale), nl2v = make_float2(nl2, nl2), ndlv = make_float2(ndl, ndl);
+  const float scd = kDrop ? scale * drop_scale : scale;
+  const float2 sc = make_float2(scd, scd), nl2v = make_float2(nl2, nl2), ndlv = make_float2(ndl, ndl);
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     uint32_t sr[64], dr[64];
@@ -43,7 +47,13 @@ __device__ __forceinline__ void dq_form_ds(uint32_t t_s, uint32_t t_dp, float sc
         p0 = (c >= a_lo && c <= e_hi) ? p0 : 0.f;
         p1 = (c + 1 >= a_lo && c + 1 <= e_hi) ? p1 : 0.f;
       }
-      const float2 d = __ffma2_rn(make_float2(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), sc, ndlv);
+      float dp0 = __uint_as_float(dr[2 * e]), dp1 = __uint_as_float(dr[2 * e + 1]);
+      if constexpr (kDrop) {
+        const uint32_t kb = km[c >> 5] >> (c & 31);
+        dp0 = (kb & 1u) ? dp0 : 0.f;
+        dp1 = (kb & 2u) ? dp1 : 0.f;
+      }
+      const float2 d = __ffma2_rn(make_float2(dp0, dp1), sc, ndlv);
       const float2 ds = __fmul2_rn(make_float2(p0, p1), d);
       pk[hf][e] = pack_bf16x2(ds.x, ds.y);
     }

@@ -20,10 +20,15 @@
 //               finally normalises O and writes out / LSE.
 // The two q tiles of a CTA share every K/V tile (same kv head), so the tensor
 // core works on one while the other's softmax runs.
+// With attention dropout (kDrop), each softmax thread draws its row's keep
+// mask of a K/V tile before that tile's S arrives, zeroes the dropped weights
+// of P (the row sum stays the undropped one) and folds the keep scale into the
+// final normalisation.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -54,7 +59,7 @@ struct FwdTmem {
   static_assert(kUsed <= 512, "tensor memory budget");
 };
 
-template <int D, int NQ, int NS, bool kMerge>
+template <int D, int NQ, int NS, bool kMerge, bool kDrop>
 __global__ void __launch_bounds__(128 + NQ * 128, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
@@ -264,6 +269,8 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
+      uint32_t km[4];  // dropout: keep bits of this row over the tile's 128 keys
+      if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
       if (!warp_wait(&s.s_full[qi], j & 1, &s.abort_flag, vstatus)) {
         ok = false;
         break;
@@ -354,7 +361,12 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         const float2 ex = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), sl2v, nmmv);
         const float p0 = fast_exp2(ex.x), p1 = fast_exp2(ex.y);
         rs2[c & 3] = __fadd2_rn(rs2[c & 3], make_float2(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
+        if constexpr (kDrop) {
+          const uint32_t kb = km[c >> 4] >> ((2 * c) & 31);
+          pk[c] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
+        } else {
+          pk[c] = pack_bf16x2(p0, p1);
+        }
       }
       const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
       const float2 r = __fadd2_rn(r01, r23);
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     } else {
       tc_fence_after();
-      float inv = l > 0.f ? 1.0f / l : 0.f;
+      float inv = l > 0.f ? (kDrop ? g.drop_scale : 1.0f) / l : 0.f;
       float lse_v = (real && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
       const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
       uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
@@ -440,7 +452,8 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
                               const int32_t* seg, const Geom& g, __nv_bfloat16* out, float* lse, int32_t* status,
                               int merge, cudaStream_t st) {
   const size_t smem = sizeof(FwdSmem<D, NQ, NS>) + 1024;  // + 1 KB to align the swizzled tiles
-  auto kern = merge ? fwd_kernel<D, NQ, NS, true> : fwd_kernel<D, NQ, NS, false>;
+  auto kern = g.drop_t ? (merge ? fwd_kernel<D, NQ, NS, true, true> : fwd_kernel<D, NQ, NS, false, true>)
+                       : (merge ? fwd_kernel<D, NQ, NS, true, false> : fwd_kernel<D, NQ, NS, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);

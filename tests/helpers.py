@@ -36,13 +36,15 @@ def make_case(w: synth.Workload, r: int, seed: int = 0, kv: tuple[int, int] | No
 
 def oracle_geom(c: dict):
     w = c["w"]
-    return oracle.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], c["window"])
+    return oracle.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], c["window"],
+                       dropout_p=c.get("dropout_p", 0.0), seed=c.get("drop_seed", 0))
 
 
 def gpu_geom(c: dict):
     from sliding_window_attention_device_gb300 import bdattn
     w = c["w"]
-    return bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], c["window"])
+    return bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], c["window"],
+                       dropout_p=c.get("dropout_p", 0.0), seed=c.get("drop_seed", 0))
 
 
 def run_gpu(c: dict, grad_dtype=torch.float32, bwd: bool = True) -> dict:

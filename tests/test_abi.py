@@ -130,7 +130,7 @@ def test_kv_layout_constants_and_validation(lib):
     consts = dict(re.findall(r"#define\s+(BD_KV_\w+)\s+(\d+)", text))
     assert int(consts["BD_KV_BHSD"]) == bdattn.KV_BHSD and int(consts["BD_KV_SBHD"]) == bdattn.KV_SBHD
     fields = re.search(r"typedef struct \{(.*?)\} bd_geom;", text, re.S).group(1)
-    names = re.findall(r"\b(?:int|float)\s+(\w+);", fields)
+    names = re.findall(r"\b(?:int|float|uint32_t)\s+(\w+);", fields)
     assert names == [n for n, _ in bdattn.Geom._fields_]
     g = bdattn.geom(1, 2, 1, 64, 256, 64, 0, 0, 256, 0, kv_layout=bdattn.KV_SBHD)
     assert bdattn.kv_shape(g) == (256, 1, 1, 64) and lib.bd_attn_seg_bytes(ctypes.byref(g)) > 0
@@ -142,3 +142,22 @@ def test_deterministic_backward_rejects_null_pointers(lib):
     g = bdattn.geom(1, 2, 1, 512, 256, 64, 0, 0, 256, 0)
     assert lib.bd_attn_bwd_deterministic(None, None, None, None, None, None, None, ctypes.byref(g), 0, None, None,
                                          None, None, None, None) == bdattn.BD_ERR_ARG
+
+
+def test_dropout_arguments_are_checked_on_the_host():
+    """dropout_p outside [0, 1), or rounding to a threshold of 2^16, and any
+    dropout at head dim 512 are refused before anything touches a device."""
+    lib = bdattn.load()
+    P = ctypes.c_void_p
+    for p in (1.0, -0.1, float("nan"), 0.99999999):
+        g = bdattn.geom(1, 2, 1, 128, 1024, 256, 256, 0, 1024, dropout_p=p, seed=3)
+        assert lib.bd_attn_fwd(P(16), P(16), P(16), P(16), ctypes.byref(g), P(16), P(16), P(16), None) == \
+            bdattn.BD_ERR_ARG, p
+        assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
+    g = bdattn.geom(1, 2, 1, 512, 1024, 256, 256, 0, 1024, dropout_p=0.1, seed=3)
+    assert lib.bd_attn_fwd(P(16), P(16), P(16), P(16), ctypes.byref(g), P(16), P(16), P(16), None) == \
+        bdattn.BD_ERR_ARG
+    assert lib.bd_attn_bwd(P(16), P(16), P(16), P(16), P(16), P(16), P(16), ctypes.byref(g), 0, P(16), P(16), P(16),
+                           P(256), P(16), None) == bdattn.BD_ERR_ARG
+    assert lib.bd_attn_bwd_deterministic(P(16), P(16), P(16), P(16), P(16), P(16), P(16), ctypes.byref(g), 0,
+                                         P(16), P(16), P(16), P(256), P(16), None) == bdattn.BD_ERR_ARG

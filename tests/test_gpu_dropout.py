@@ -1,0 +1,126 @@
+"""Attention dropout on the GPU against the fp64 oracle, element by element.
+
+blockdiag_cp.kernels `_cp_blockdiag_varlen` takes `dropout_p` (attention
+dropout probability). Both sides draw the keep decision of every (query head,
+query position, key position) pair from Philox-4x32-10 with the counter
+(key / 8, query, head, batch row) and the seed, each from its own code; so
+out, lse, dq, dk and dv must agree within the parity bar for the same p and
+seed, as without dropout. The cases cover head dims 64 / 128 / 256, K/V
+buffers that start at a position that is not a multiple of 8 (the decisions
+follow global positions), windows, GQA groups of 1 to 4, both gradient dtypes,
+the fixed-order (deterministic) backward, and K/V in chunks merged in the
+forward's epilogue.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (assert_close, assert_close_bf16, assert_lse, make_case, oracle_geom, real_rows, run_gpu)
+from sliding_window_attention_device_gb300 import bdattn, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def W(key, B, Hq, Hkv, D, S, cp, layout, window=0, kv="full"):
+    return synth.Workload(key, key, B=B, Hq=Hq, Hkv=Hkv, D=D, S=S, cp_size=cp, layout=layout, window=window,
+                          ranks=tuple(range(cp)), kv=kv)
+
+
+CASES = [
+    ("d128_g2", W("a", 2, 4, 2, 128, 1280, 4, ("uniform", 20, 300, 40)), 2),
+    ("d128_g4_needed", W("b", 2, 8, 2, 128, 1536, 4, ("uniform", 30, 500, 0), kv="needed"), 3),
+    ("d64_g1_window", W("c", 1, 3, 3, 64, 1024, 2, ("uniform", 50, 400, 70), window=100), 1),
+    ("d256_g2_window", W("d", 1, 4, 2, 256, 1280, 4, ("uniform", 100, 600, 30), window=150, kv="prefix"), 3),
+    ("d256_g1_needed", W("e", 2, 2, 2, 256, 1024, 4, ("uniform", 20, 300, 10), kv="needed"), 2),
+]
+
+
+def _case(w, r, p, seed):
+    c = make_case(w, r, seed=r + 7)
+    c["dropout_p"], c["drop_seed"] = p, seed
+    return c
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5])
+@pytest.mark.parametrize("name,w,r", CASES, ids=[c[0] for c in CASES])
+def test_dropout_fwd_bwd_parity(name, w, r, p):
+    c = _case(w, r, p, seed=0x5EED_0000_0000_0000 + r)
+    if w.kv == "needed":
+        assert c["kv_offset"] % 8 != 0 or name == "d256_g1_needed", "want a K/V buffer off the 8-key grid"
+    g = oracle_geom(c)
+    out, lse = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], g)
+    dq, dk, dv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], g)
+    real = real_rows(c)
+    for gd in (torch.float32, torch.bfloat16):
+        res = run_gpu(c, grad_dtype=gd)
+        assert res["status_word"] == 0, f"status {res['status_word']:#x}"
+        assert_close(f"{name} p{p} out", res["out"], out)
+        assert_lse(res["lse"], lse, real)
+        close = assert_close if gd == torch.float32 else assert_close_bf16
+        close(f"{name} p{p} dq {gd}", res["dq"], dq)
+        close(f"{name} p{p} dk {gd}", res["dk"], dk)
+        close(f"{name} p{p} dv {gd}", res["dv"], dv)
+
+
+def test_dropout_changes_the_result_and_follows_the_seed():
+    w = CASES[0][1]
+    base = run_gpu(_case(w, 2, 0.0, 0))
+    a = run_gpu(_case(w, 2, 0.5, 1))
+    b = run_gpu(_case(w, 2, 0.5, 1))
+    c = run_gpu(_case(w, 2, 0.5, 2))
+    assert torch.equal(a["out"], b["out"]) and torch.equal(a["dk"], b["dk"])
+    assert not torch.equal(a["out"], c["out"])
+    assert not torch.equal(a["out"], base["out"])
+    assert torch.equal(a["lse"], base["lse"])  # the normaliser is the undropped softmax's
+
+
+@pytest.mark.parametrize("name", ["d128_g4_needed", "d256_g2_window"])
+def test_dropout_deterministic_backward(name):
+    w, r = next((c[1], c[2]) for c in CASES if c[0] == name)
+    c = _case(w, r, 0.3, 99)
+    res = run_gpu(c)
+    g = oracle_geom(c)
+    dq, dk, dv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], g)
+    dev = torch.device("cuda")
+    q, k, v, do = (c[n].to(dev) for n in ("q", "k", "v", "do"))
+    got = [bdattn.bd_attn_bwd_deterministic(do, q, k, v, res["out"], res["lse"], res["seg"], res["g"],
+                                            res["status"]) for _ in range(2)]
+    torch.cuda.synchronize()
+    assert int(res["status"].item()) == 0
+    for t0, t1 in zip(*got):
+        assert torch.equal(t0, t1)  # bitwise reproducible
+    assert_close(f"{name} det dq", got[0][0], dq)
+    assert_close(f"{name} det dk", got[0][1], dk)
+    assert_close(f"{name} det dv", got[0][2], dv)
+    assert torch.equal(got[0][1], res["dk"]) and torch.equal(got[0][2], res["dv"])
+
+
+def test_dropout_chunked_forward_merge():
+    """K/V in three chunks, each merged into the running (out, lse) in the
+    forward's epilogue, equals the oracle's one-piece dropout forward."""
+    w = W("f", 1, 4, 2, 128, 1536, 4, ("uniform", 40, 900, 20))
+    r = 3
+    c = _case(w, r, 0.25, 1234)
+    g = oracle_geom(c)
+    out_ref, lse_ref = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], g)
+    dev = torch.device("cuda")
+    doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
+    q = c["q"].to(dev)
+    status = bdattn.new_status(dev)
+    out = torch.empty(w.B, w.Hq, w.L, w.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
+    cuts = (0, 301, 777, w.S)  # chunk starts off the 8-key grid
+    for n in range(3):
+        a, e = cuts[n], cuts[n + 1]
+        gc = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, r * w.L, a, e - a, dropout_p=0.25, seed=1234)
+        segc, _ = bdattn.bd_attn_seg_build_chunk(doc, gc, status=status)
+        kc, vc = c["k"][:, :, a:e].contiguous().to(dev), c["v"][:, :, a:e].contiguous().to(dev)
+        if n == 0:
+            bdattn.bd_attn_fwd(q, kc, vc, segc, gc, status, out=out, lse=lse)
+        else:
+            bdattn.bd_attn_fwd_merge(q, kc, vc, segc, gc, status, out, lse)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_close("chunked dropout out", out, out_ref)
+    assert_lse(lse, lse_ref, real_rows(c))
