@@ -463,8 +463,12 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
   return cudaGetLastError();
 }
 
+cudaError_t launch_fwd256(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
+                          const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st);
+
 // Two query heads of one GQA group per CTA when the group size is even and
-// D <= 128 (tensor memory: 2 x (128 + D) columns); one otherwise.
+// D <= 128 (tensor memory: 2 x (128 + D) columns); one otherwise. D = 256 has
+// its own kernel with K / V streamed in halves (fwd256_kernel.cu).
 cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const int32_t* seg,
                        const Geom& g, void* out, float* lse, int32_t* status, int merge, cudaStream_t st) {
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
@@ -477,7 +481,7 @@ cudaError_t launch_fwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
       return pairs ? launch_one<128, 2, 2>(mq, mk, mv, seg, g, o, lse, status, merge, st)
                    : launch_one<128, 1, 2>(mq, mk, mv, seg, g, o, lse, status, merge, st);
     case 256:
-      return launch_one<256, 1, 1>(mq, mk, mv, seg, g, o, lse, status, merge, st);
+      return launch_fwd256(mq, mk, mv, seg, g, out, lse, status, merge, st);
     default:
       return cudaErrorInvalidValue;
   }
