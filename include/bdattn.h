@@ -70,13 +70,13 @@ typedef struct {
   int window;     /* left window W (> 0: also require p - s < W); <= 0: none */
   float scale;    /* softmax scale; <= 0 means D^-0.5 */
   int kv_layout;  /* layout of k, v, dk, dv: BD_KV_BHSD (0) or BD_KV_SBHD (1) */
-  float dropout_p;  /* attention dropout probability, 0 <= p < 1 (0: none); see below */
+  float dropout_p;  /* chance of dropping an attention weight, 0 <= p < 1 (0: none); see below */
   uint32_t seed_lo; /* dropout seed: low and high 32 bits (the Philox key) */
   uint32_t seed_hi;
 } bd_geom;
 
 /* Attention dropout (blockdiag_cp.kernels, `_cp_blockdiag_varlen` argument
- * `dropout_p`: attention dropout probability). Inverted dropout on the
+ * `dropout_p`, the chance that an attention weight is dropped). Inverted dropout on the
  * softmax probabilities: out_p = sum_s P_ps Z_ps v_s with Z_ps = 0 (dropped)
  * or 2^16 / (2^16 - T) (kept); the LSE is that of the undropped softmax, and
  * the backward takes the same Z (dV = sum_p P Z dO, dS = P (Z dP - delta)).

@@ -25,7 +25,7 @@
  *  [A.lse]     gemma4_moe.cp_attention, `_scatter_lse`: LSE is -inf on rows
  *              that take no part.
  *  [K.drop]    blockdiag_cp.kernels, `_cp_blockdiag_varlen`, argument
- *              `dropout_p` (attention dropout probability); the same argument
+ *              `dropout_p` (the chance that an attention weight is dropped); the same argument
  *              on the FlashAttention varlen helpers and ring-attention
  *              functions of gemma4_moe.cp_attention. Read as inverted
  *              dropout on the attention probabilities: each allowed P_ps is

@@ -2,11 +2,12 @@
 // key position) pair, drawn on the device.
 //
 // blockdiag_cp.kernels `_cp_blockdiag_varlen` (and the FlashAttention varlen
-// helpers of gemma4_moe.cp_attention) take `dropout_p`, the attention dropout
-// probability. It acts on the softmax probabilities P: a weight is kept with
-// probability 1 - p and then scaled by the inverse of that probability
-// (inverted dropout), so the forward output is sum_s P_ps Z_ps v_s with
-// Z in {0, scale}; the softmax normaliser and the LSE stay the undropped ones.
+// helpers of gemma4_moe.cp_attention) take `dropout_p`, the chance that an
+// attention weight is dropped. It acts on the softmax probabilities P: a
+// weight is kept with probability 1 - p and then scaled by the inverse of that
+// probability (inverted dropout), so the forward output is sum_s P_ps Z_ps v_s
+// with Z in {0, scale}; the softmax normaliser and the LSE stay the undropped
+// ones.
 //
 // The random bits come from Philox-4x32-10 (Salmon, Moraes, Dror, Shaw,
 // "Parallel random numbers: as easy as 1, 2, 3", SC'11), a counter-based

@@ -1,7 +1,7 @@
 """Attention dropout on the GPU against the fp64 oracle, element by element.
 
-blockdiag_cp.kernels `_cp_blockdiag_varlen` takes `dropout_p` (attention
-dropout probability). Both sides draw the keep decision of every (query head,
+blockdiag_cp.kernels `_cp_blockdiag_varlen` takes `dropout_p`, the chance that
+an attention weight is dropped. Both sides draw the keep decision of every (query head,
 query position, key position) pair from Philox-4x32-10 with the counter
 (key / 8, query, head, batch row) and the seed, each from its own code; so
 out, lse, dq, dk and dv must agree within the parity bar for the same p and
@@ -10,13 +10,20 @@ buffers that start at a position that is not a multiple of 8 (the decisions
 follow global positions), windows, GQA groups of 1 to 4, both gradient dtypes,
 the fixed-order (deterministic) backward, and K/V in chunks merged in the
 forward's epilogue.
+
+Tolerance: the parity bar times the keep scale 2^16 / (2^16 - T). Every term
+a dropout run adds is an undropped term times Z <= that scale, and the terms
+the GPU rounds to bf16 before its tensor-core products (dS, for dK and dQ)
+carry that factor, so their rounding errors do too: x1.11 at p = 0.1, x2 at
+p = 0.5.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from helpers import (assert_close, assert_close_bf16, assert_lse, make_case, oracle_geom, real_rows, run_gpu)
+from helpers import (MAX_ABS, MEAN_ABS, assert_close, assert_close_bf16, assert_lse, make_case, oracle_geom,
+                     real_rows, run_gpu)
 from sliding_window_attention_device_gb300 import bdattn, synth
 
 pytestmark = pytest.mark.gpu
@@ -42,6 +49,14 @@ def _case(w, r, p, seed):
     return c
 
 
+def _bar(p):
+    """(max-abs, mean-abs) for dropout probability p: the parity bar times the
+    keep scale."""
+    t = int(np.floor(p * 65536 + 0.5))
+    k = 65536.0 / (65536 - t)
+    return MAX_ABS * k, MEAN_ABS * k
+
+
 @pytest.mark.parametrize("p", [0.1, 0.5])
 @pytest.mark.parametrize("name,w,r", CASES, ids=[c[0] for c in CASES])
 def test_dropout_fwd_bwd_parity(name, w, r, p):
@@ -52,15 +67,16 @@ def test_dropout_fwd_bwd_parity(name, w, r, p):
     out, lse = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], g)
     dq, dk, dv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], g)
     real = real_rows(c)
+    mx, mn = _bar(p)
     for gd in (torch.float32, torch.bfloat16):
         res = run_gpu(c, grad_dtype=gd)
         assert res["status_word"] == 0, f"status {res['status_word']:#x}"
-        assert_close(f"{name} p{p} out", res["out"], out)
+        assert_close(f"{name} p{p} out", res["out"], out, mx, mn)
         assert_lse(res["lse"], lse, real)
         close = assert_close if gd == torch.float32 else assert_close_bf16
-        close(f"{name} p{p} dq {gd}", res["dq"], dq)
-        close(f"{name} p{p} dk {gd}", res["dk"], dk)
-        close(f"{name} p{p} dv {gd}", res["dv"], dv)
+        close(f"{name} p{p} dq {gd}", res["dq"], dq, mx, mn)
+        close(f"{name} p{p} dk {gd}", res["dk"], dk, mx, mn)
+        close(f"{name} p{p} dv {gd}", res["dv"], dv, mx, mn)
 
 
 def test_dropout_changes_the_result_and_follows_the_seed():
@@ -90,9 +106,10 @@ def test_dropout_deterministic_backward(name):
     assert int(res["status"].item()) == 0
     for t0, t1 in zip(*got):
         assert torch.equal(t0, t1)  # bitwise reproducible
-    assert_close(f"{name} det dq", got[0][0], dq)
-    assert_close(f"{name} det dk", got[0][1], dk)
-    assert_close(f"{name} det dv", got[0][2], dv)
+    mx, mn = _bar(0.3)
+    assert_close(f"{name} det dq", got[0][0], dq, mx, mn)
+    assert_close(f"{name} det dk", got[0][1], dk, mx, mn)
+    assert_close(f"{name} det dv", got[0][2], dv, mx, mn)
     assert torch.equal(got[0][1], res["dk"]) and torch.equal(got[0][2], res["dv"])
 
 
@@ -122,5 +139,5 @@ def test_dropout_chunked_forward_merge():
             bdattn.bd_attn_fwd_merge(q, kc, vc, segc, gc, status, out, lse)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert_close("chunked dropout out", out, out_ref)
+    assert_close("chunked dropout out", out, out_ref, *_bar(0.25))
     assert_lse(lse, lse_ref, real_rows(c))

@@ -1,7 +1,7 @@
 """Pins of the oracle's attention dropout against things other than itself.
 
-The pages expose `dropout_p` (blockdiag_cp.kernels `_cp_blockdiag_varlen`:
-attention dropout probability) and say no more. The oracle reads it as
+The pages expose `dropout_p` (blockdiag_cp.kernels `_cp_blockdiag_varlen`),
+the chance that an attention weight is dropped, and say no more. The oracle reads it as
 inverted dropout on the attention probabilities, with the keep decisions drawn
 by Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) from a counter of
 (key position / 8, query position, query head, batch row) and a 64-bit seed:
