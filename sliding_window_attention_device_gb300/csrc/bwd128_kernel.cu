@@ -9,10 +9,14 @@
 // costs 5 x (D/16 or 8) instructions.
 //
 // Work units are (128-row K/V tile, kv head) pairs, longest first (the
-// backward work list). The grid is persistent -- at most one CTA per SM --
-// and CTA c takes units c, 2G - 1 - c, 2G + c, ... of the list (G CTAs, a
-// snake order that evens out the longest-first lengths); for each it loops
-// over the group's query heads and the 128-row q tiles that attend its keys.
+// backward work list). The grid is persistent -- at most one CTA per SM:
+// CTA c starts with unit c and then claims the next unclaimed unit of the
+// list from a counter in the workspace (zeroed by the zero-fill launch just
+// before), so units are handed out longest first as CTAs free up, as the
+// hardware would dispatch one CTA per unit; the loading warp claims and
+// publishes each unit to the other roles through a four-slot ring. For a unit
+// the CTA loops over the group's query heads and the 128-row q tiles that
+// attend its keys.
 // The roles run ahead across units: K / V of the next unit load as soon as
 // the last product of this one is done (`kv_empty`) and its first S^T / dP^T
 // are formed while the P / dS warps still write this unit's dK / dV, whose
@@ -63,6 +67,8 @@ struct Ctl {
   float delta[2][kQ];
   uint64_t kv_full, kv_empty, q_full[2], q_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
+  uint64_t unit_full[4];  // unit ring: slot k % 4 holds the CTA's k-th unit (-1: no more)
+  int unit[4];
   uint32_t tmem_base;
   int abort_flag;
   int n_units, skip;
@@ -101,11 +107,6 @@ __device__ __forceinline__ Unit decode_unit(const int32_t* seg, const Geom& g, i
   return x;
 }
 
-// The r-th unit of CTA c of n CTAs (snake order), or -1 past the list's end.
-__device__ __forceinline__ int unit_of(int r, int c, int n, int n_units) {
-  const int u = r * n + ((r & 1) ? n - 1 - c : c);
-  return u < n_units ? u : -1;
-}
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
@@ -132,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
                   const float* __restrict__ delta, float* __restrict__ dq_acc,
-                  void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
+                  void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int* __restrict__ sched,
+                  int32_t* status) {
   pdl_begin();
   using T = Tiles<D>;
   constexpr int kChunks = T::kChunks;
@@ -172,10 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, 256);
     mbar_init(&s.mma_drain, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&s.unit_full[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (s.skip || unit_of(0, blockIdx.x, gridDim.x, s.n_units) < 0) return;
+  if (s.skip || static_cast<int>(blockIdx.x) >= s.n_units) return;
   const int n_units = s.n_units;
   const int G = g.G;
   const bool is_pds = (warp >= 4 && warp < 8) || warp >= 12;
@@ -198,6 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  // the CTA's k-th unit from the ring (-1: no more units, or the wait gave up);
+  // a whole warp (or the single MMA thread) waits
+  auto next_unit = [&](int k, bool warpwide) {
+    const bool ok = warpwide ? warp_wait(&s.unit_full[k & 3], (k >> 2) & 1, &s.abort_flag, vstatus)
+                             : pipe_wait(&s.unit_full[k & 3], (k >> 2) & 1, &s.abort_flag, vstatus);
+    return ok ? *reinterpret_cast<volatile int*>(&s.unit[k & 3]) : -1;
+  };
+
   if (warp == 2) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
@@ -217,13 +228,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int IT = 0, ku = 0;  // iterations and units loaded by this CTA
     bool stop = false;
-    for (int r = 0; !stop; ++r) {
-      const int u = unit_of(r, blockIdx.x, gridDim.x, n_units);
+    // the k-th unit: the CTA's own index first, then claimed from the counter,
+    // published to the other roles. Unit k + 1 is published once this warp
+    // has issued unit k's loads, i.e. once the MMA thread has finished unit
+    // k - 1 (so the P / dS warps are at unit k - 1 or later and the dQ warps
+    // at unit k): slot (k + 1) % 4 last held unit k - 3, which every role has
+    // left.
+    int u = static_cast<int>(blockIdx.x);
+    auto publish = [&](int k, int unit) {
+      if (lane == 0) {
+        s.unit[k & 3] = unit;
+        mbar_arrive(&s.unit_full[k & 3]);
+      }
+      __syncwarp();
+    };
+    publish(0, u);
+    for (int k = 0; !stop; ++k) {
+      if (k > 0) {
+        int claimed = 0;
+        if (lane == 0) claimed = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
+        claimed = __shfl_sync(0xffffffffu, claimed, 0);
+        u = claimed < n_units ? claimed : -1;
+        publish(k, u);
+      }
       if (u < 0) break;
       const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) {
+      if (!x.ok) {  // a corrupt table: this CTA stops, publishing no further unit
         if (lane == 0) atomicOr(status, BD_STATUS_BOUNDS);
-        continue;
+        break;
       }
       // K / V of this unit once the previous unit's products are done with them
       if (ku > 0 && !warp_wait(&s.kv_empty, (ku - 1) & 1, &s.abort_flag, vstatus)) break;
@@ -308,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
       bool ok = true;
       int IT = 0, ku = 0;  // iterations and units issued by this CTA
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of(r, blockIdx.x, gridDim.x, n_units);
+      for (int k = 0; ok; ++k) {
+        const int u = next_unit(k, false);
         if (u < 0) break;
         const Unit x = decode_unit(seg, g, u);
-        if (!x.ok) continue;
+        if (!x.ok) break;  // a corrupt table: the loading warp stops here too
         const int n_it = G * x.nq;
         // this unit's first S^T and dP^T: S^T's columns were last read by the
         // previous unit's final dV product (issued before); dP^T's hold the
@@ -397,11 +429,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sc_dp = kDrop ? g.scale * g.drop_scale : g.scale;
     bool ok = true;
     int IT = 0, ku = 0;  // iterations and units done by this CTA
-    for (int ru = 0; ok; ++ru) {
-      const int u = unit_of(ru, blockIdx.x, gridDim.x, n_units);
+    for (int k = 0; ok; ++k) {
+      const int u = next_unit(k, true);
       if (u < 0) break;
       const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) continue;
+      if (!x.ok) break;  // a corrupt table: the loading warp stops here too
       const int b = x.b, kt = x.kt, hk = x.hk, n_real = x.n_real;
       const int n_it = G * x.nq;
       const int j = kt * kTile + r;
@@ -561,11 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool active = (warp & 3) * 32 < D;  // D = 64: lanes 64..127 hold nothing useful
     bool ok = true;
     int IT = 0;  // iterations read out by this CTA
-    for (int ru = 0; ok; ++ru) {
-      const int u = unit_of(ru, blockIdx.x, gridDim.x, n_units);
+    for (int k = 0; ok; ++k) {
+      const int u = next_unit(k, true);
       if (u < 0) break;
       const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) continue;
+      if (!x.ok) break;  // a corrupt table: the loading warp stops here too
       const int n_it = G * x.nq;
       int gq = 0, qt = 0;
       for (int it = 0; it < n_it; ++it, ++IT) {
@@ -624,7 +656,7 @@ namespace {
 template <int D>
 cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
                       const int32_t* seg, const Geom& g, const float* lse, const float* delta, float* dq_acc,
-                      void* dk, void* dv, int bf16, int32_t* status, cudaStream_t st) {
+                      void* dk, void* dv, int bf16, int* sched, int32_t* status, cudaStream_t st) {
   constexpr size_t need = bwd128_smem_bytes<D>();
   // request the layout plus alignment slack, up to the per-block maximum; the
   // kernel verifies at run time that its 1024-byte-aligned layout fits
@@ -650,7 +682,7 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
   const long long grid = units < n_sm ? units : n_sm;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, mq, mdo,
-      mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status); le != cudaSuccess) return le;
+      mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace
@@ -658,11 +690,11 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
 // Backward main kernel for D = 64 / 128 (q and dout maps must use 128-row boxes).
 cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
-                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
-                               cudaStream_t st) {
+                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int* sched,
+                               int32_t* status, cudaStream_t st) {
   switch (g.D) {
-    case 64: return launch128<64>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
-    case 128: return launch128<128>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 64: return launch128<64>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status, st);
+    case 128: return launch128<128>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status, st);
     default: return cudaErrorInvalidValue;
   }
 }
