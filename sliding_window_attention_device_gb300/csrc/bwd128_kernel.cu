@@ -8,20 +8,8 @@
 // ~65% of the tensor rate on this part), so each 128 x 128 (key, query) tile
 // costs 5 x (D/16 or 8) instructions.
 //
-// Work units are (128-row K/V tile, kv head) pairs, longest first (the
-// backward work list). The grid is persistent -- at most one CTA per SM:
-// CTA c starts with unit c and then claims the next unclaimed unit of the
-// list from a counter in the workspace (zeroed by the zero-fill launch just
-// before), so units are handed out longest first as CTAs free up, as the
-// hardware would dispatch one CTA per unit; the loading warp claims and
-// publishes each unit to the other roles through a four-slot ring. For a unit
-// the CTA loops over the group's query heads and the 128-row q tiles that
-// attend its keys.
-// The roles run ahead across units: K / V of the next unit load as soon as
-// the last product of this one is done (`kv_empty`) and its first S^T / dP^T
-// are formed while the P / dS warps still write this unit's dK / dV, whose
-// tensor-memory columns the next unit's dV / dK products take only once read
-// (`acc_empty`). Per-iteration barriers run on a CTA-wide iteration count.
+// One CTA per (128-row K/V tile, kv head), longest first; it loops over the
+// group's query heads and the 128-row q tiles that attend its keys.
 //   tensor memory  [0,128)   S^T = K Q^T, then P^T (bf16, packed in place)
 //                  [128,256) dP^T = V dO^T, then dQ^T = K^T dS^T
 //                  [256,384) dV += P^T dO        [384,512) dK += dS^T Q
@@ -65,48 +53,16 @@ struct Tiles {
 struct Ctl {
   float lse2[2][kQ];  // per q row: lse * log2(e)
   float delta[2][kQ];
-  uint64_t kv_full, kv_empty, q_full[2], q_empty[2];
+  uint64_t kv_full, q_full[2], q_empty[2];
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
-  uint64_t unit_full[4];  // unit ring: slot k % 4 holds the CTA's k-th unit (-1: no more)
-  int unit[4];
   uint32_t tmem_base;
   int abort_flag;
-  int n_units, skip;
+  int b, kt, q_lo, nq, n_real, skip, mode;
 };
 
-// One work unit: (K/V tile kt of batch row b, kv head hk) and the 128-row q
-// tiles [q_lo, q_lo + nq) that attend it.
-struct Unit {
-  int b, kt, hk, q_lo, nq, n_real;
-  bool ok;
-};
-
-// Unit u of the work list (u < n_att * Hkv), from the segment table. Every
-// role decodes its units itself, so all see the same values; `ok` false
-// (a corrupt table) makes every role skip the unit.
-__device__ __forceinline__ Unit decode_unit(const int32_t* seg, const Geom& g, int u) {
-  Unit x;
-  const int item = u / g.Hkv;
-  x.hk = u - item * g.Hkv;
-  const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
-  bool ok = wi >= 0 && wi < g.B * g.nkt;
-  x.b = ok ? wi / g.nkt : 0;
-  x.kt = ok ? wi % g.nkt : 0;
-  const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + x.b * BD_SEG_HDR_WORDS;
-  ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
-       hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
-       hdr[kHdrSfull] == g.S_full;
-  x.n_real = hdr[BD_SEG_N_REAL];
-  const int32_t* qr = seg + g.off[BD_SEG_OFF_KT_QRANGE] + (x.b * g.nkt + x.kt) * 2;
-  const int qlo = qr[0], qhi = qr[1];
-  // an attended tile has a non-empty q range
-  ok = ok && x.n_real >= 0 && x.n_real <= g.L && qlo >= 0 && qhi <= x.n_real && qlo < qhi;
-  x.q_lo = ok ? qlo / kQ : 0;
-  x.nq = ok ? (qhi - 1) / kQ - qlo / kQ + 1 : 0;
-  x.ok = ok;
-  return x;
-}
-
+// What a CTA does, from its position in the backward work list.
+constexpr int kModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
+constexpr int kModeWork = 1;  // an attended K/V tile
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
@@ -133,8 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const int32_t* __restrict__ seg, const Geom g, const float* __restrict__ lse,
                   const float* __restrict__ delta, float* __restrict__ dq_acc,
-                  void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int* __restrict__ sched,
-                  int32_t* status) {
+                  void* __restrict__ dk, void* __restrict__ dv, int grads_bf16, int32_t* status) {
   pdl_begin();
   using T = Tiles<D>;
   constexpr int kChunks = T::kChunks;
@@ -148,18 +103,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   T& t = *reinterpret_cast<T*>(smem_raw + align_off);
   Ctl& s = *reinterpret_cast<Ctl*>(smem_raw + align_off + sizeof(T));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hk = blockIdx.x % g.Hkv;
   volatile int* vstatus = status;
 
+  const int item = blockIdx.x / g.Hkv;
   if (tid == 0) {
-    // the attended K/V tiles lead the work list
+    // the attended K/V tiles lead the work list; the grid must cover them
     const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
-    const bool ok = n_att >= 0 && n_att <= g.B * g.nkt;
+    int mode = kModeIdle;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv)
+      atomicOr(status, BD_STATUS_BOUNDS);
+    else
+      mode = item < n_att ? kModeWork : kModeIdle;
+    s.mode = mode;
+  }
+  __syncthreads();
+  if (s.mode != kModeWork) return;
+
+  if (tid == 0) {
+    const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
+    int ok = wi >= 0 && wi < g.B * g.nkt;
+    const int b = ok ? wi / g.nkt : 0, kt = ok ? wi % g.nkt : 0;
+    const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+    ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
+         hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
+         hdr[kHdrSfull] == g.S_full;
+    const int n_real = hdr[BD_SEG_N_REAL];
+    const int32_t* qr = seg + g.off[BD_SEG_OFF_KT_QRANGE] + (b * g.nkt + kt) * 2;
+    const int qlo = qr[0], qhi = qr[1];
+    // an attended tile has a non-empty q range
+    ok = ok && n_real >= 0 && n_real <= g.L && qlo >= 0 && qhi <= n_real && qlo < qhi;
     if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
-    s.n_units = ok ? n_att * g.Hkv : 0;
+    s.b = b;
+    s.kt = kt;
+    s.q_lo = qlo / kQ;
+    s.nq = qhi > qlo ? (qhi - 1) / kQ - qlo / kQ + 1 : 0;
+    s.n_real = n_real;
     s.skip = (!ok || *vstatus != 0) ? 1 : 0;
     s.abort_flag = 0;
     mbar_init(&s.kv_full, 1);
-    mbar_init(&s.kv_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.q_full[i], 1);
       mbar_init(&s.q_empty[i], 1);
@@ -174,13 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s.acc_full, 1);
     mbar_init(&s.acc_empty, 256);
     mbar_init(&s.mma_drain, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&s.unit_full[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (s.skip || static_cast<int>(blockIdx.x) >= s.n_units) return;
-  const int n_units = s.n_units;
+  if (s.skip) return;
+  const int b = s.b, kt = s.kt, q_lo = s.q_lo, nq = s.nq, n_real = s.n_real;
   const int G = g.G;
+  const int n_it = G * nq;  // iteration it: query head hk*G + it / nq, q tile q_lo + it % nq
+  // dK / dV row j of this (batch row, kv head): kv_row(g, b, hk, j)
   const bool is_pds = (warp >= 4 && warp < 8) || warp >= 12;
   const int half = warp >= 12 ? 1 : 0;
 
@@ -201,14 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  // the CTA's k-th unit from the ring (-1: no more units, or the wait gave up);
-  // a whole warp (or the single MMA thread) waits
-  auto next_unit = [&](int k, bool warpwide) {
-    const bool ok = warpwide ? warp_wait(&s.unit_full[k & 3], (k >> 2) & 1, &s.abort_flag, vstatus)
-                             : pipe_wait(&s.unit_full[k & 3], (k >> 2) & 1, &s.abort_flag, vstatus);
-    return ok ? *reinterpret_cast<volatile int*>(&s.unit[k & 3]) : -1;
-  };
-
   if (warp == 2) {
     tmem_alloc(&s.tmem_base, 512);
     tmem_relinquish();
@@ -225,98 +200,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_dout);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&s.kv_full, 2 * kChunks * kChunk);
+      for (int c = 0; c < kChunks; ++c) {
+        tma_load_3d(t.k[c], &tm_k, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
+        tma_load_3d(t.v[c], &tm_v, &s.kv_full, c * 64, g.kv_tm ? b * g.Hkv + hk : kt * kTile, g.kv_tm ? kt * kTile : b * g.Hkv + hk);
+      }
     }
-    int IT = 0, ku = 0;  // iterations and units loaded by this CTA
-    bool stop = false;
-    // the k-th unit: the CTA's own index first, then claimed from the counter,
-    // published to the other roles. Unit k + 1 is published once this warp
-    // has issued unit k's loads, i.e. once the MMA thread has finished unit
-    // k - 1 (so the P / dS warps are at unit k - 1 or later and the dQ warps
-    // at unit k): slot (k + 1) % 4 last held unit k - 3, which every role has
-    // left.
-    int u = static_cast<int>(blockIdx.x);
-    auto publish = [&](int k, int unit) {
-      if (lane == 0) {
-        s.unit[k & 3] = unit;
-        mbar_arrive(&s.unit_full[k & 3]);
+    int issued = 0, gq = 0, qt = 0;  // (head, q tile) of iteration `it`
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it & 1;
+      const int h = hk * G + gq, q0 = (q_lo + qt) * kQ;
+      // fetch this tile's per-row values before waiting for the free stage
+      float l2[4], dl[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = q0 + lane + 32 * e;
+        l2[e] = 0.f;
+        dl[e] = 0.f;
+        if (i < n_real) {
+          const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
+          l2[e] = lse[row] * 1.4426950408889634f;
+          dl[e] = delta[row] * g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
+        }
+      }
+      if (it >= 2 && !warp_wait(&s.q_empty[st], ((it >> 1) - 1) & 1, &s.abort_flag, vstatus)) break;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s.lse2[st][lane + 32 * e] = l2[e];
+        s.delta[st][lane + 32 * e] = dl[e];
       }
       __syncwarp();
-    };
-    publish(0, u);
-    for (int k = 0; !stop; ++k) {
-      if (k > 0) {
-        int claimed = 0;
-        if (lane == 0) claimed = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
-        claimed = __shfl_sync(0xffffffffu, claimed, 0);
-        u = claimed < n_units ? claimed : -1;
-        publish(k, u);
-      }
-      if (u < 0) break;
-      const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) {  // a corrupt table: this CTA stops, publishing no further unit
-        if (lane == 0) atomicOr(status, BD_STATUS_BOUNDS);
-        break;
-      }
-      // K / V of this unit once the previous unit's products are done with them
-      if (ku > 0 && !warp_wait(&s.kv_empty, (ku - 1) & 1, &s.abort_flag, vstatus)) break;
-      const int pl = x.b * g.Hkv + x.hk;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&s.kv_full, 2 * kChunks * kChunk);
+        mbar_arrive_expect_tx(&s.q_full[st], 2 * kChunks * kChunk);
         for (int c = 0; c < kChunks; ++c) {
-          tma_load_3d(t.k[c], &tm_k, &s.kv_full, c * 64, g.kv_tm ? pl : x.kt * kTile, g.kv_tm ? x.kt * kTile : pl);
-          tma_load_3d(t.v[c], &tm_v, &s.kv_full, c * 64, g.kv_tm ? pl : x.kt * kTile, g.kv_tm ? x.kt * kTile : pl);
+          tma_load_3d(t.q[st][c], &tm_q, &s.q_full[st], c * 64, q0, b * g.Hq + h);
+          tma_load_3d(t.dout[st][c], &tm_dout, &s.q_full[st], c * 64, q0, b * g.Hq + h);
         }
       }
-      ++ku;
-      const int n_it = G * x.nq;  // iteration it: query head hk*G + it / nq, q tile q_lo + it % nq
-      int gq = 0, qt = 0;
-      for (int it = 0; it < n_it; ++it, ++IT) {
-        const int st = IT & 1;
-        const int h = x.hk * G + gq, q0 = (x.q_lo + qt) * kQ;
-        // fetch this tile's per-row values before waiting for the free stage
-        float l2[4], dl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = q0 + lane + 32 * e;
-          l2[e] = 0.f;
-          dl[e] = 0.f;
-          if (i < x.n_real) {
-            const size_t row = (static_cast<size_t>(x.b) * g.Hq + h) * g.L + i;
-            l2[e] = lse[row] * 1.4426950408889634f;
-            dl[e] = delta[row] * g.scale;  // dS is formed pre-scaled: scale * P (dP - delta)
-          }
-        }
-        if (IT >= 2 && !warp_wait(&s.q_empty[st], ((IT >> 1) - 1) & 1, &s.abort_flag, vstatus)) {
-          stop = true;
-          break;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          s.lse2[st][lane + 32 * e] = l2[e];
-          s.delta[st][lane + 32 * e] = dl[e];
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&s.q_full[st], 2 * kChunks * kChunk);
-          for (int c = 0; c < kChunks; ++c) {
-            tma_load_3d(t.q[st][c], &tm_q, &s.q_full[st], c * 64, q0, x.b * g.Hq + h);
-            tma_load_3d(t.dout[st][c], &tm_dout, &s.q_full[st], c * 64, q0, x.b * g.Hq + h);
-          }
-        }
-        if (++qt == x.nq) {
-          qt = 0;
-          ++gq;
-        }
+      ++issued;
+      if (++qt == nq) {
+        qt = 0;
+        ++gq;
       }
     }
     if (lane == 0) {
-      if (stop || s.abort_flag) {
+      if (issued < n_it) {
         s.abort_flag = 1;
         atomicOr(status, BD_STATUS_TIMEOUT);
       }
-      // no copy into this CTA's shared memory may still be in flight at exit
-      if (ku > 0) mbar_wait_drain(&s.kv_full, (ku - 1) & 1);
-      for (int i = (IT > 2 ? IT - 2 : 0); i < IT; ++i) mbar_wait_drain(&s.q_full[i & 1], (i >> 1) & 1);
+      mbar_wait_drain(&s.kv_full, 0);
+      for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it) mbar_wait_drain(&s.q_full[it & 1], (it >> 1) & 1);
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
@@ -338,78 +271,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
-      bool ok = true;
-      int IT = 0, ku = 0;  // iterations and units issued by this CTA
-      for (int k = 0; ok; ++k) {
-        const int u = next_unit(k, false);
-        if (u < 0) break;
-        const Unit x = decode_unit(seg, g, u);
-        if (!x.ok) break;  // a corrupt table: the loading warp stops here too
-        const int n_it = G * x.nq;
-        // this unit's first S^T and dP^T: S^T's columns were last read by the
-        // previous unit's final dV product (issued before); dP^T's hold the
-        // previous unit's final dQ^T until the dQ warps have read it
-        if (!wait(&s.kv_full, ku & 1) || !wait(&s.q_full[IT & 1], (IT >> 1) & 1)) { ok = false; break; }
+      bool ok = wait(&s.kv_full, 0) && wait(&s.q_full[0], 0);
+      if (ok) {
         tc_fence_after();
-        issue_t(kColS, a_k, a_q + (IT & 1) * kStage);
+        issue_t(kColS, a_k, a_q);
         umma_commit(&s.s_full);
-        if (kDq && IT > 0 && !wait(&s.dq_empty, (IT - 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_t(kColDp, a_v, a_do + (IT & 1) * kStage);
+        issue_t(kColDp, a_v, a_do);
         umma_commit(&s.dp_full);
-        for (int it = 0; it < n_it; ++it, ++IT) {
-          const int st = IT & 1;
-          // dV += P^T dO : P^T (bf16) sits in tensor memory over S^T, q columns
-          // 0-63 at column 0 and 64-127 at column 64 (each half over its own S^T)
-          if (!wait(&s.p_full, IT & 1)) { ok = false; break; }
-          // the first product of a unit overwrites dV / dK: the previous
-          // unit's values must have been read out
-          if (it == 0 && ku > 0 && !wait(&s.acc_empty, (ku - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it & 1;
+        // dV += P^T dO : P^T (bf16) sits in tensor memory over S^T, q columns
+        // 0-63 at column 0 and 64-127 at column 64 (each half over its own S^T)
+        if (!wait(&s.p_full, it & 1)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < kQ / 16; ++ks) {
-            const uint32_t a_col = kColS + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
-            umma_ts(tbase + kColDv, tbase + a_col, desc_at(dMN, a_do + st * kStage + ks * 2048), idDKV,
-                    (it > 0 || ks > 0) ? 1u : 0u);
-          }
-          // S^T of the next tile can go in now (the dV product above was issued
-          // first, so it reads P^T before S^T is overwritten)
-          if (it + 1 < n_it) {
-            if (!wait(&s.q_full[st ^ 1], ((IT + 1) >> 1) & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_t(kColS, a_k, a_q + (st ^ 1) * kStage);
-            umma_commit(&s.s_full);
-          }
-          // dQ^T = K^T dS^T into the dP^T columns (dS is written, so dP^T was read)
-          if (!wait(&s.ds_full, IT & 1)) { ok = false; break; }
-          tc_fence_after();
-          if constexpr (kDq) {
-#pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks)
-              umma_ss(tbase + kColDp, desc_at(dMN, a_k + ks * 2048), desc_at(dMN, a_ds + ks * 2048), idDQ,
-                      ks > 0 ? 1u : 0u);
-            umma_commit(&s.dq_full);
-          }
-          // dK += dS^T Q
-#pragma unroll
-          for (int ks = 0; ks < kQ / 16; ++ks)
-            umma_ss(tbase + kColDk, desc_at(dKm, a_ds + (ks >> 2) * kChunk + (ks & 3) * 32),
-                    desc_at(dMN, a_q + st * kStage + ks * 2048), idDKV, (it > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&s.ds_empty);
-          umma_commit(&s.q_empty[st]);
-          if (it + 1 == n_it) {
-            umma_commit(&s.acc_full);  // dV / dK of this unit are complete
-            umma_commit(&s.kv_empty);  // and K / V are no longer read
-          }
-          // dP^T of the next tile once dQ^T has been read out of those columns
-          if (it + 1 < n_it) {
-            if (kDq && !wait(&s.dq_empty, IT & 1)) { ok = false; break; }
-            tc_fence_after();
-            issue_t(kColDp, a_v, a_do + (st ^ 1) * kStage);
-            umma_commit(&s.dp_full);
-          }
+        for (int ks = 0; ks < kQ / 16; ++ks) {
+          const uint32_t a_col = kColS + (ks < 4 ? ks * 8 : 64 + (ks - 4) * 8);
+          umma_ts(tbase + kColDv, tbase + a_col, desc_at(dMN, a_do + st * kStage + ks * 2048), idDKV,
+                  (it > 0 || ks > 0) ? 1u : 0u);
         }
-        ++ku;
+        // S^T of the next tile can go in now (the dV product above was issued
+        // first, so it reads P^T before S^T is overwritten)
+        if (it + 1 < n_it) {
+          if (!wait(&s.q_full[st ^ 1], ((it + 1) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_t(kColS, a_k, a_q + (st ^ 1) * kStage);
+          umma_commit(&s.s_full);
+        }
+        // dQ^T = K^T dS^T into the dP^T columns (dS is written, so dP^T was read)
+        if (!wait(&s.ds_full, it & 1)) { ok = false; break; }
+        tc_fence_after();
+        if constexpr (kDq) {
+#pragma unroll
+          for (int ks = 0; ks < kTile / 16; ++ks)
+            umma_ss(tbase + kColDp, desc_at(dMN, a_k + ks * 2048), desc_at(dMN, a_ds + ks * 2048), idDQ,
+                    ks > 0 ? 1u : 0u);
+          umma_commit(&s.dq_full);
+        }
+        // dK += dS^T Q
+#pragma unroll
+        for (int ks = 0; ks < kQ / 16; ++ks)
+          umma_ss(tbase + kColDk, desc_at(dKm, a_ds + (ks >> 2) * kChunk + (ks & 3) * 32),
+                  desc_at(dMN, a_q + st * kStage + ks * 2048), idDKV, (it > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(&s.ds_empty);
+        umma_commit(&s.q_empty[st]);
+        if (it + 1 == n_it) umma_commit(&s.acc_full);
+        // dP^T of the next tile once dQ^T has been read out of those columns
+        if (it + 1 < n_it) {
+          if (kDq && !wait(&s.dq_empty, it & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_t(kColDp, a_v, a_do + (st ^ 1) * kStage);
+          umma_commit(&s.dp_full);
+        }
       }
       if (!ok) {
         s.abort_flag = 1;
@@ -422,165 +336,153 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------- P and dS (key rows; one half of the q columns)
     const int r = (warp & 3) * 32 + lane;  // key row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int j = kt * kTile + r;
     const int c0 = half * 64;  // first q column of this half
     const float sl2 = g.scale * 1.4426950408889634f;
     uint8_t* ds_row = t.ds[half] + r * 128;
+    // A real row p >= key s attends s iff p lies in the document that contains
+    // s (documents are contiguous runs) and, with a window, p - s < W: rows
+    // [s, min(doc_end(s), s + W)) of the real rows. doc_end(s) is fixed for
+    // the CTA; find it once from cu_q.
+    const int key = g.kv_offset + j;
+    int doc_end = -0x40000000;  // keys no local row attends
+    {
+      const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+      const int32_t* cu_q = seg + g.off[BD_SEG_OFF_CU_Q] + b * (g.L + 1);
+      const int n_seg = hdr[BD_SEG_N_SEG];
+      if (n_seg > 0 && key >= hdr[BD_SEG_S_FIRST] && key < hdr[BD_SEG_REAL_END]) {
+        int k = 0;  // the last segment with row_offset + cu_q[k] <= key
+        if (key >= g.row_offset) {
+          int a = 0, e = n_seg - 1;
+          while (a < e) {
+            const int mid = (a + e + 1) >> 1;
+            if (g.row_offset + cu_q[mid] <= key) a = mid; else e = mid - 1;
+          }
+          k = a;
+        }
+        doc_end = g.row_offset + cu_q[k + 1];
+      }
+    }
+    const int row_end = min(doc_end, g.window > 0 ? key + g.window : 0x3fffffff);
     // dropout: scale * keep scale multiplies a kept dP (a dropped one is zero)
     const float sc_dp = kDrop ? g.scale * g.drop_scale : g.scale;
     bool ok = true;
-    int IT = 0, ku = 0;  // iterations and units done by this CTA
-    for (int k = 0; ok; ++k) {
-      const int u = next_unit(k, true);
-      if (u < 0) break;
-      const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) break;  // a corrupt table: the loading warp stops here too
-      const int b = x.b, kt = x.kt, hk = x.hk, n_real = x.n_real;
-      const int n_it = G * x.nq;
-      const int j = kt * kTile + r;
-      // A real row p >= key s attends s iff p lies in the document that contains
-      // s (documents are contiguous runs) and, with a window, p - s < W: rows
-      // [s, min(doc_end(s), s + W)) of the real rows. doc_end(s) is fixed for
-      // the unit; find it once from cu_q.
-      const int key = g.kv_offset + j;
-      int doc_end = -0x40000000;  // keys no local row attends
-      {
-        const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
-        const int32_t* cu_q = seg + g.off[BD_SEG_OFF_CU_Q] + b * (g.L + 1);
-        const int n_seg = hdr[BD_SEG_N_SEG];
-        if (n_seg > 0 && key >= hdr[BD_SEG_S_FIRST] && key < hdr[BD_SEG_REAL_END]) {
-          int k = 0;  // the last segment with row_offset + cu_q[k] <= key
-          if (key >= g.row_offset) {
-            int a = 0, e = n_seg - 1;
-            while (a < e) {
-              const int mid = (a + e + 1) >> 1;
-              if (g.row_offset + cu_q[mid] <= key) a = mid; else e = mid - 1;
-            }
-            k = a;
-          }
-          doc_end = g.row_offset + cu_q[k + 1];
-        }
+    int qt = 0, gq = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it & 1;
+      const int q0 = (q_lo + qt) * kQ;
+      uint64_t km = 0;  // dropout: keep bits of this key over the half's 64 q columns
+      if constexpr (kDrop)
+        km = key_keep_mask<8>(g, b, hk * G + gq, g.row_offset + q0 + c0, g.kv_offset + kt * kTile + (warp & 3) * 32,
+                              lane);
+      if (++qt == nq) {
+        qt = 0;
+        ++gq;
       }
-      const int row_end = min(doc_end, g.window > 0 ? key + g.window : 0x3fffffff);
-      int qt = 0, gq = 0;
-      for (int it = 0; it < n_it; ++it, ++IT) {
-        const int st = IT & 1;
-        const int q0 = (x.q_lo + qt) * kQ;
-        uint64_t km = 0;  // dropout: keep bits of this key over the half's 64 q columns
-        if constexpr (kDrop)
-          km = key_keep_mask<8>(g, b, hk * G + gq, g.row_offset + q0 + c0, g.kv_offset + kt * kTile + (warp & 3) * 32,
-                                lane);
-        if (++qt == x.nq) {
-          qt = 0;
-          ++gq;
-        }
-        if (!warp_wait(&s.q_full[st], (IT >> 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-        if (!warp_wait(&s.s_full, IT & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-        tc_fence_after();
-        // q columns [c_lo, c_hi) of this tile attend the key (relative to c0)
-        const int row0 = g.row_offset + q0;
-        const int c_lo = max(0, key - row0) - c0;
-        const int c_hi = min(min(kQ, n_real - q0), row_end - row0) - c0;
-        float p[64];  // P in fp32, kept for dS
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t sr[32];
-          tmem_ld32(tbase + lane_off + kColS + c0 + 32 * h2, sr);
-          tmem_wait_ld();
-          const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st] + c0 + 32 * h2);
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 l = l4[c4];
-            const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 32 * h2 + 4 * c4 + e;
-              const float pe = fast_exp2(__uint_as_float(sr[4 * c4 + e]) * sl2 - lv[e]);
-              p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
-            }
-          }
-          // packed bf16 P of these 32 q columns over S^T columns this half has read
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = 32 * h2 + 2 * e;
-            if constexpr (kDrop)
-              pk[e] = pack_bf16x2(((km >> c) & 1u) ? p[c] : 0.f, ((km >> (c + 1)) & 1u) ? p[c + 1] : 0.f);
-            else
-              pk[e] = pack_bf16x2(p[c], p[c + 1]);
-          }
-          tmem_st16(tbase + lane_off + kColS + c0 + 16 * h2, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.p_full);
-
-        if (!warp_wait(&s.dp_full, IT & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-        tc_fence_after();
-        // the previous tile's dK / dQ products must be done reading dS^T
-        if (IT > 0 && !warp_wait(&s.ds_empty, (IT - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-#pragma unroll
-        for (int h4 = 0; h4 < 4; ++h4) {  // 16 q columns at a time
-          uint32_t sr[16];
-          tmem_ld16(tbase + lane_off + kColDp + c0 + 16 * h4, sr);
-          tmem_wait_ld();
-          const float4* d4 = reinterpret_cast<const float4*>(s.delta[st] + c0 + 16 * h4);
-          uint32_t dsk[8];  // dS of 16 q columns, bf16 pairs
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const float4 dl = d4[c4];
-            const int c = 16 * h4 + 4 * c4;
-            float dp[4] = {__uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1]),
-                           __uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])};
-            if constexpr (kDrop) {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) dp[e] = ((km >> (c + e)) & 1u) ? dp[e] : 0.f;
-            }
-            dsk[2 * c4] = pack_bf16x2(p[c] * fmaf(dp[0], sc_dp, -dl.x), p[c + 1] * fmaf(dp[1], sc_dp, -dl.y));
-            dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(dp[2], sc_dp, -dl.z), p[c + 3] * fmaf(dp[3], sc_dp, -dl.w));
-          }
-          // 32 B of this key row of dS^T (128B-swizzled K-major layout)
-#pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2) {
-            const int c16 = 2 * h4 + k2;
-            *reinterpret_cast<uint4*>(ds_row + ((c16 ^ (r & 7)) << 4)) =
-                make_uint4(dsk[4 * k2], dsk[4 * k2 + 1], dsk[4 * k2 + 2], dsk[4 * k2 + 3]);
-          }
-        }
-        tc_fence_before();  // the dP^T reads above complete before dQ^T may overwrite those columns
-        fence_proxy_async_smem();
-        mbar_arrive(&s.ds_full);
-      }
-      if (!ok) break;
-      // write this thread's dK / dV row (its half of the columns), then hand
-      // the accumulator columns to the next unit
-      if (!warp_wait(&s.acc_full, ku & 1, &s.abort_flag, vstatus)) {
-        ok = false;
-        break;
-      }
+      if (!warp_wait(&s.q_full[st], (it >> 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      if (!warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
-        uint32_t vv[32];
-        float f[32];
-        tmem_ld32(tbase + lane_off + kColDv + c, vv);
-        tmem_wait_ld();
-        if (j < g.S_kv) {
-          const float dvs = kDrop ? g.drop_scale : 1.0f;  // dropout: the keep scale of P^T
+      // q columns [c_lo, c_hi) of this tile attend the key (relative to c0)
+      const int row0 = g.row_offset + q0;
+      const int c_lo = max(0, key - row0) - c0;
+      const int c_hi = min(min(kQ, n_real - q0), row_end - row0) - c0;
+      float p[64];  // P in fp32, kept for dS
 #pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * dvs;
-          store_row(dv, kv_row(g, b, hk, j) * D + c, f);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t sr[32];
+        tmem_ld32(tbase + lane_off + kColS + c0 + 32 * h2, sr);
+        tmem_wait_ld();
+        const float4* l4 = reinterpret_cast<const float4*>(s.lse2[st] + c0 + 32 * h2);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 l = l4[c4];
+          const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 32 * h2 + 4 * c4 + e;
+            const float pe = fast_exp2(__uint_as_float(sr[4 * c4 + e]) * sl2 - lv[e]);
+            p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+          }
         }
-        tmem_ld32(tbase + lane_off + kColDk + c, vv);
-        tmem_wait_ld();
-        if (j < g.S_kv) {
+        // packed bf16 P of these 32 q columns over S^T columns this half has read
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
-          store_row(dk, kv_row(g, b, hk, j) * D + c, f);
+        for (int e = 0; e < 16; ++e) {
+          const int c = 32 * h2 + 2 * e;
+          if constexpr (kDrop)
+            pk[e] = pack_bf16x2(((km >> c) & 1u) ? p[c] : 0.f, ((km >> (c + 1)) & 1u) ? p[c + 1] : 0.f);
+          else
+            pk[e] = pack_bf16x2(p[c], p[c + 1]);
+        }
+        tmem_st16(tbase + lane_off + kColS + c0 + 16 * h2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full);
+
+      if (!warp_wait(&s.dp_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      tc_fence_after();
+      // the previous tile's dK / dQ products must be done reading dS^T
+      if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+#pragma unroll
+      for (int h4 = 0; h4 < 4; ++h4) {  // 16 q columns at a time
+        uint32_t sr[16];
+        tmem_ld16(tbase + lane_off + kColDp + c0 + 16 * h4, sr);
+        tmem_wait_ld();
+        const float4* d4 = reinterpret_cast<const float4*>(s.delta[st] + c0 + 16 * h4);
+        uint32_t dsk[8];  // dS of 16 q columns, bf16 pairs
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const float4 dl = d4[c4];
+          const int c = 16 * h4 + 4 * c4;
+          float dp[4] = {__uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1]), __uint_as_float(sr[4 * c4 + 2]),
+                         __uint_as_float(sr[4 * c4 + 3])};
+          if constexpr (kDrop) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dp[e] = ((km >> (c + e)) & 1u) ? dp[e] : 0.f;
+          }
+          dsk[2 * c4] = pack_bf16x2(p[c] * fmaf(dp[0], sc_dp, -dl.x), p[c + 1] * fmaf(dp[1], sc_dp, -dl.y));
+          dsk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(dp[2], sc_dp, -dl.z), p[c + 3] * fmaf(dp[3], sc_dp, -dl.w));
+        }
+        // 32 B of this key row of dS^T (128B-swizzled K-major layout)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int c16 = 2 * h4 + k2;
+          *reinterpret_cast<uint4*>(ds_row + ((c16 ^ (r & 7)) << 4)) =
+              make_uint4(dsk[4 * k2], dsk[4 * k2 + 1], dsk[4 * k2 + 2], dsk[4 * k2 + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&s.acc_empty);
-      ++ku;
+      tc_fence_before();  // the dP^T reads above complete before dQ^T may overwrite those columns
+      fence_proxy_async_smem();
+      mbar_arrive(&s.ds_full);
+    }
+    if (ok) {
+      // write this thread's dK / dV row (its half of the columns)
+      if (!warp_wait(&s.acc_full, 0, &s.abort_flag, vstatus)) {
+        ok = false;
+      } else {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+          uint32_t vv[32];
+          float f[32];
+          tmem_ld32(tbase + lane_off + kColDv + c, vv);
+          tmem_wait_ld();
+          if (j < g.S_kv) {
+            const float dvs = kDrop ? g.drop_scale : 1.0f;  // dropout: the keep scale of P^T
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]) * dvs;
+            store_row(dv, kv_row(g, b, hk, j) * D + c, f);
+          }
+          tmem_ld32(tbase + lane_off + kColDk + c, vv);
+          tmem_wait_ld();
+          if (j < g.S_kv) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(vv[e]);  // dS was pre-scaled
+            store_row(dk, kv_row(g, b, hk, j) * D + c, f);
+          }
+        }
+      }
     }
     if (!ok) {
       s.abort_flag = 1;
@@ -592,48 +494,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const bool active = (warp & 3) * 32 < D;  // D = 64: lanes 64..127 hold nothing useful
     bool ok = true;
-    int IT = 0;  // iterations read out by this CTA
-    for (int k = 0; ok; ++k) {
-      const int u = next_unit(k, true);
-      if (u < 0) break;
-      const Unit x = decode_unit(seg, g, u);
-      if (!x.ok) break;  // a corrupt table: the loading warp stops here too
-      const int n_it = G * x.nq;
-      int gq = 0, qt = 0;
-      for (int it = 0; it < n_it; ++it, ++IT) {
-        const int h = x.hk * G + gq, q0 = (x.q_lo + qt) * kQ;
-        if (++qt == x.nq) {
-          qt = 0;
-          ++gq;
+    int gq = 0, qt = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int h = hk * G + gq, q0 = (q_lo + qt) * kQ;
+      if (++qt == nq) {
+        qt = 0;
+        ++gq;
+      }
+      if (!warp_wait(&s.dq_full, it & 1, &s.abort_flag, vstatus)) { ok = false; break; }
+      tc_fence_after();
+      // two halves of 64 q columns; the columns are released after the second read
+      float* base = dq_acc + ((static_cast<size_t>(b) * g.Hq + h) * g.L + q0) * D + r;
+      const int cmax = min(kQ, n_real - q0);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t qv[64];
+        if (active) {
+          tmem_ld32(tbase + lane_off + kColDp + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+          tmem_ld32(tbase + lane_off + kColDp + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+          tmem_wait_ld();
         }
-        if (!warp_wait(&s.dq_full, IT & 1, &s.abort_flag, vstatus)) { ok = false; break; }
-        tc_fence_after();
-        // two halves of 64 q columns; the columns are released after the second read
-        float* base = dq_acc + ((static_cast<size_t>(x.b) * g.Hq + h) * g.L + q0) * D + r;
-        const int cmax = min(kQ, x.n_real - q0);
+        if (hh == 1) {
+          tc_fence_before();
+          mbar_arrive(&s.dq_empty);
+        }
+        if (active) {
+          // these warps issue one red per value and nothing else: a full
+          // tile takes the loop without a per-value row check
+          if (cmax >= kQ) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t qv[64];
-          if (active) {
-            tmem_ld32(tbase + lane_off + kColDp + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
-            tmem_ld32(tbase + lane_off + kColDp + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
-            tmem_wait_ld();
-          }
-          if (hh == 1) {
-            tc_fence_before();
-            mbar_arrive(&s.dq_empty);
-          }
-          if (active) {
-            // these warps issue one red per value and nothing else: a full
-            // tile takes the loop without a per-value row check
-            if (cmax >= kQ) {
+            for (int c = 0; c < 64; ++c) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
+          } else {
 #pragma unroll
-              for (int c = 0; c < 64; ++c) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
-            } else {
-#pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (64 * hh + c < cmax) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
-            }
+            for (int c = 0; c < 64; ++c)
+              if (64 * hh + c < cmax) red_add(base + static_cast<size_t>(64 * hh + c) * D, __uint_as_float(qv[c]));
           }
         }
       }
@@ -656,7 +550,7 @@ namespace {
 template <int D>
 cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk, const CUtensorMap& mv,
                       const int32_t* seg, const Geom& g, const float* lse, const float* delta, float* dq_acc,
-                      void* dk, void* dv, int bf16, int* sched, int32_t* status, cudaStream_t st) {
+                      void* dk, void* dv, int bf16, int32_t* status, cudaStream_t st) {
   constexpr size_t need = bwd128_smem_bytes<D>();
   // request the layout plus alignment slack, up to the per-block maximum; the
   // kernel verifies at run time that its 1024-byte-aligned layout fits
@@ -672,17 +566,13 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
                        : (dq_acc ? bwd128_kernel<D, true, false> : bwd128_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM at most (shared and tensor memory allow one),
-  // no more than the units some local row can reach by position
-  int n_sm = 0;
-  e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  // only tiles some local row can reach by position get a working CTA; with
+  // none reachable, B CTAs per kv head still zero dK / dV
   const int reach = kv_tiles_reachable(g);
-  const long long units = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
-  const long long grid = units < n_sm ? units : n_sm;
+  const long long grid = static_cast<long long>(g.B) * (reach > 0 ? reach : 1) * g.Hkv;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, mq, mdo,
-      mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status); le != cudaSuccess) return le;
+      mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace
@@ -690,11 +580,11 @@ cudaError_t launch128(const CUtensorMap& mq, const CUtensorMap& mdo, const CUten
 // Backward main kernel for D = 64 / 128 (q and dout maps must use 128-row boxes).
 cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
-                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int* sched,
-                               int32_t* status, cudaStream_t st) {
+                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
+                               cudaStream_t st) {
   switch (g.D) {
-    case 64: return launch128<64>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status, st);
-    case 128: return launch128<128>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, sched, status, st);
+    case 64: return launch128<64>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 128: return launch128<128>(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
   }
 }

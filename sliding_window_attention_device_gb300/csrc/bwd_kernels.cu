@@ -685,10 +685,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // kernels' CTAs for those tiles exit at once and this streaming kernel writes
 // the zeros (every (tile, kv head) pair past the attended ones in the work list).
 __global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const int32_t* __restrict__ seg, const Geom g, void* dk,
-                                                          void* dv, int grads_bf16, int* sched, int32_t* status) {
+                                                          void* dv, int grads_bf16, int32_t* status) {
   pdl_begin();
-  // the persistent backward main kernel that follows claims its units from this counter
-  if (sched != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
   if (n_att < 0 || n_att > g.B * g.nkt) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, BD_STATUS_BOUNDS);
@@ -726,13 +724,7 @@ cudaError_t launch_main_d(const CUtensorMap& mq, const CUtensorMap& mdo, const C
 // Workspace: fp32 dq accumulator [B,Hq,L,D], then fp32 delta [B,Hq,L].
 size_t bwd_workspace_bytes(const Geom& g) {
   const size_t rows = static_cast<size_t>(g.B) * g.Hq * g.L;
-  return align256(rows * g.D * 4) + align256(rows * 4) + 256;  // + the unit counter of the persistent kernels
-}
-
-// The word the persistent backward kernel claims its units from (zeroed by the zero-fill kernel).
-static int* ws_sched(const Geom& g, void* workspace) {
-  const size_t rows = static_cast<size_t>(g.B) * g.Hq * g.L;
-  return reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + align256(rows * g.D * 4) + align256(rows * 4));
+  return align256(rows * g.D * 4) + align256(rows * 4);
 }
 
 static float* ws_delta(const Geom& g, void* workspace) {
@@ -785,8 +777,8 @@ cudaError_t launch_pre(const Geom& g, const void* dout, const void* out, void* w
 
 cudaError_t launch_bwd128_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
-                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int* sched,
-                               int32_t* status, cudaStream_t st);
+                               const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
+                               cudaStream_t st);
 cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
@@ -808,15 +800,14 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
     const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
     const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
     if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
-        ws_sched(g, workspace), status); le != cudaSuccess) return le;
+        status); le != cudaSuccess) return le;
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   switch (g.D) {
     case 64:
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
-      return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, ws_sched(g, workspace),
-                                status, st);
+      return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 256:
       return launch_main_d<256, true>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 512:  // the head dim of the outputs split over four CTAs (bwd512_kernel.cu)
@@ -835,15 +826,15 @@ cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, 
   const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
   const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
   if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
-      ws_sched(g, workspace), status); le != cudaSuccess) return le;
+      status); le != cudaSuccess) return le;
   if (g.D == 512)
     return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
                               st);
   if (g.D == 256)  // the dq map is not read without the dq products
     return launch_main_d<256, false>(mq, mdo, mk, mv, mq, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16,
                                      status, st);
-  return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16,
-                            ws_sched(g, workspace), status, st);
+  return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
+                            st);
 }
 
 // K4b: dq = the accumulator (already scaled) in the gradient dtype.

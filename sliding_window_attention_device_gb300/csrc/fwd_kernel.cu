@@ -6,14 +6,8 @@
 // times V; LSE = natural-log sum-exp (gemma4_moe.cp_attention `_scatter_lse`:
 // -inf on rows that take no part). Padding rows return zeros.
 //
-// Design (GB300): work units are (128-row q tile, pair of query heads of the
-// same GQA group), the q tiles with the most K/V tiles first. The grid is
-// persistent -- at most one CTA per SM, CTA c taking units c, 2G - 1 - c,
-// 2G + c, ... of the list (G CTAs, snake order) -- and its roles run ahead
-// across units: the next unit's Q loads once this unit's last S products are
-// done (`q_empty`), its first S products run while the softmax warps write
-// this unit's out, and its first PV products wait only for O to be read out
-// (`o_free`). Per-tile barriers run on a CTA-wide K/V tile count.
+// Design (GB300): one CTA per (128-row q tile, pair of query heads of the same
+// GQA group); the work list puts the q tiles with the most K/V tiles first.
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of the tile's
 //               contiguous K/V range through an NS-stage ring (128B swizzle).
 //   warp 1      one thread issues tcgen05.mma: S = Q K^T into TMEM, and
@@ -46,13 +40,14 @@ struct FwdSmem {
   alignas(1024) uint8_t q[NQ][kChunks][kChunkBytes];
   alignas(1024) uint8_t k[NS][kChunks][kChunkBytes];
   alignas(1024) uint8_t v[NS][kChunks][kChunkBytes];
-  uint64_t q_full, q_empty;
+  uint64_t q_full;
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[NQ], p_full[NQ], o_done[NQ], o_free[NQ];
+  uint64_t s_full[NQ], p_full[NQ], o_done[NQ];
   uint64_t mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int skip;
+  // work item, decoded by thread 0
+  int b, qt, kt_lo, nk, n_real, skip;
 };
 
 template <int D, int NQ>
@@ -63,48 +58,6 @@ struct FwdTmem {
   static constexpr int kCols = kUsed <= 32 ? 32 : kUsed <= 64 ? 64 : kUsed <= 128 ? 128 : kUsed <= 256 ? 256 : 512;
   static_assert(kUsed <= 512, "tensor memory budget");
 };
-
-// One work unit: q tile qt of batch row b for query heads h0 .. h0 + NQ - 1,
-// against K/V tiles [kt_lo, kt_lo + nk).
-struct FwdUnit {
-  int b, qt, h0, kt_lo, nk, n_real;
-  bool ok;
-};
-
-// Unit u (< B * nqt * Hq / nq_per_cta) of the forward work list: q tiles with
-// the most K/V tiles first, the head groups of a q tile adjacent. Every role
-// decodes its units itself, so all see the same values; `ok` false (a corrupt
-// table) makes every role skip the unit.
-__device__ __forceinline__ FwdUnit decode_fwd_unit(const int32_t* seg, const Geom& g, int u, int nq_per_cta) {
-  FwdUnit x;
-  const int n_pairs = g.Hq / nq_per_cta;
-  const int item = u / n_pairs;
-  x.h0 = (u - item * n_pairs) * nq_per_cta;
-  const int wi = seg[g.off[BD_SEG_OFF_FWD_WORK] + item];
-  bool ok = wi >= 0 && wi < g.B * g.nqt;
-  x.b = ok ? wi / g.nqt : 0;
-  x.qt = ok ? wi % g.nqt : 0;
-  const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + x.b * BD_SEG_HDR_WORDS;
-  ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
-       hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
-       hdr[kHdrSfull] == g.S_full;
-  x.n_real = hdr[BD_SEG_N_REAL];
-  const int32_t* kr = seg + g.off[BD_SEG_OFF_QT_KRANGE] + (x.b * g.nqt + x.qt) * 2;
-  const int kt_lo = kr[0], kt_hi = kr[1];
-  const int nk = kt_hi >= kt_lo ? kt_hi - kt_lo + 1 : 0;
-  ok = ok && x.n_real >= 0 && x.n_real <= g.L && (nk == 0 || (kt_lo >= 0 && kt_hi < g.nkt));
-  x.kt_lo = ok ? kt_lo : 0;
-  x.nk = ok ? nk : 0;
-  x.ok = ok;
-  return x;
-}
-
-// The r-th unit of CTA c of n CTAs (snake order over the longest-first list),
-// or -1 past its end.
-__device__ __forceinline__ int fwd_unit_of(int r, int c, int n, int n_units) {
-  const int u = r * n + ((r & 1) ? n - 1 - c : c);
-  return u < n_units ? u : -1;
-}
 
 template <int D, int NQ, int NS, bool kMerge, bool kDrop>
 __global__ void __launch_bounds__(128 + NQ * 128, 1)
@@ -119,11 +72,31 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
   // 1024-byte aligned base, derived from smem_raw so the compiler keeps the shared address space
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_units = g.B * g.nqt * (g.Hq / NQ);
+  const int n_pairs = g.Hq / NQ;
+  const int pair = blockIdx.x % n_pairs;
   volatile int* vstatus = status;
 
   if (tid == 0) {
-    s.skip = *vstatus != 0 ? 1 : 0;
+    const int item = blockIdx.x / n_pairs;
+    const int wi = seg[g.off[BD_SEG_OFF_FWD_WORK] + item];
+    int ok = wi >= 0 && wi < g.B * g.nqt;
+    const int b = ok ? wi / g.nqt : 0, qt = ok ? wi % g.nqt : 0;
+    const int32_t* hdr = seg + g.off[BD_SEG_OFF_HDR] + b * BD_SEG_HDR_WORDS;
+    ok = ok && hdr[kHdrMagic] == kSegMagic && hdr[kHdrRowOffset] == g.row_offset && hdr[kHdrL] == g.L &&
+         hdr[kHdrKvOffset] == g.kv_offset && hdr[kHdrSkv] == g.S_kv && hdr[kHdrWindow] == g.window &&
+         hdr[kHdrSfull] == g.S_full;
+    const int n_real = hdr[BD_SEG_N_REAL];
+    const int32_t* kr = seg + g.off[BD_SEG_OFF_QT_KRANGE] + (b * g.nqt + qt) * 2;
+    const int kt_lo = kr[0], kt_hi = kr[1];
+    const int nk = kt_hi >= kt_lo ? kt_hi - kt_lo + 1 : 0;
+    ok = ok && n_real >= 0 && n_real <= g.L && (nk == 0 || (kt_lo >= 0 && kt_hi < g.nkt));
+    if (!ok) atomicOr(status, BD_STATUS_BOUNDS);
+    s.b = b;
+    s.qt = qt;
+    s.kt_lo = kt_lo;
+    s.nk = nk;
+    s.n_real = n_real;
+    s.skip = (!ok || *vstatus != 0) ? 1 : 0;
     s.abort_flag = 0;
     for (int i = 0; i < NS; ++i) {
       mbar_init(&s.k_full[i], 1);
@@ -135,15 +108,33 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       mbar_init(&s.s_full[i], 1);
       mbar_init(&s.p_full[i], 128);
       mbar_init(&s.o_done[i], 1);
-      mbar_init(&s.o_free[i], 128);
     }
     mbar_init(&s.q_full, 1);
-    mbar_init(&s.q_empty, 1);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (s.skip || fwd_unit_of(0, blockIdx.x, gridDim.x, n_units) < 0) return;
+  if (s.skip) return;
+  const int b = s.b, qt = s.qt, kt_lo = s.kt_lo, nk = s.nk, n_real = s.n_real;
+  const int h0 = pair * NQ, hk = h0 / g.G;
+
+  if (nk == 0) {
+    // No row of this q tile sees a key: zeros and -inf (merging: a running
+    // result is kept, an empty one set to zeros and -inf).
+    if (tid >= 128) {
+      const int qi = (tid - 128) >> 7, r = (tid - 128) & 127;
+      const int i = qt * kTile + r;
+      if (i < g.L) {
+        const size_t row = (static_cast<size_t>(b) * g.Hq + h0 + qi) * g.L + i;
+        if (!kMerge || lse[row] == -INFINITY) {
+          uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
+          for (int c = 0; c < D / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+          lse[row] = -INFINITY;
+        }
+      }
+    }
+    return;
+  }
 
   if (warp == 2) {
     tmem_alloc(&s.tmem_base, TM::kCols);
@@ -159,53 +150,32 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    int T = 0, ku = 0;  // K/V tiles and units (with keys) loaded by this CTA
+    mbar_arrive_expect_tx(&s.q_full, NQ * kChunks * Smem::kChunkBytes);
+    for (int qi = 0; qi < NQ; ++qi)
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.q[qi][c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h0 + qi);
     int k_issued = 0, v_issued = 0;
-    bool stop = false;
-    for (int r = 0; !stop; ++r) {
-      const int u = fwd_unit_of(r, blockIdx.x, gridDim.x, n_units);
-      if (u < 0) break;
-      const FwdUnit x = decode_fwd_unit(seg, g, u, NQ);
-      if (!x.ok) {
-        atomicOr(status, BD_STATUS_BOUNDS);
-        continue;
-      }
-      if (x.nk == 0) continue;
-      const int hk = x.h0 / g.G;
-      // Q of this unit once the previous unit's S products are done with it
-      if (ku > 0 && !pipe_wait(&s.q_empty, (ku - 1) & 1, &s.abort_flag, vstatus)) break;
-      mbar_arrive_expect_tx(&s.q_full, NQ * kChunks * Smem::kChunkBytes);
-      for (int qi = 0; qi < NQ; ++qi)
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(s.q[qi][c], &tm_q, &s.q_full, c * 64, x.qt * kTile, x.b * g.Hq + x.h0 + qi);
-      ++ku;
-      for (int j = 0; j < x.nk; ++j, ++T) {
-        const int st = T % NS, n = T / NS;
-        const int row = (x.kt_lo + j) * kTile, pl = x.b * g.Hkv + hk;
-        if (T >= NS && !pipe_wait(&s.k_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) {
-          stop = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&s.k_full[st], kChunks * Smem::kChunkBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(s.k[st][c], &tm_k, &s.k_full[st], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
-        ++k_issued;
-        if (T >= NS && !pipe_wait(&s.v_empty[st], (n - 1) & 1, &s.abort_flag, vstatus)) {
-          stop = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&s.v_full[st], kChunks * Smem::kChunkBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(s.v[st][c], &tm_v, &s.v_full[st], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
-        ++v_issued;
-      }
+    for (int j = 0; j < nk; ++j) {
+      const int st = j % NS, n = j / NS;
+      if (j >= NS && !pipe_wait(&s.k_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
+        break;
+      mbar_arrive_expect_tx(&s.k_full[st], kChunks * Smem::kChunkBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.k[st][c], &tm_k, &s.k_full[st], c * 64, g.kv_tm ? b * g.Hkv + hk : (kt_lo + j) * kTile, g.kv_tm ? (kt_lo + j) * kTile : b * g.Hkv + hk);
+      ++k_issued;
+      if (j >= NS && !pipe_wait(&s.v_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
+        break;
+      mbar_arrive_expect_tx(&s.v_full[st], kChunks * Smem::kChunkBytes);
+      for (int c = 0; c < kChunks; ++c)
+        tma_load_3d(s.v[st][c], &tm_v, &s.v_full[st], c * 64, g.kv_tm ? b * g.Hkv + hk : (kt_lo + j) * kTile, g.kv_tm ? (kt_lo + j) * kTile : b * g.Hkv + hk);
+      ++v_issued;
     }
-    if (stop || s.abort_flag) {
+    if (v_issued < nk) {
       s.abort_flag = 1;
       atomicOr(status, BD_STATUS_TIMEOUT);
     }
     // make sure no copy into this CTA's shared memory is still in flight at exit
-    if (ku > 0) mbar_wait_drain(&s.q_full, (ku - 1) & 1);
+    mbar_wait_drain(&s.q_full, 0);
     for (int j = (k_issued > NS ? k_issued - NS : 0); j < k_issued; ++j) mbar_wait_drain(&s.k_full[j % NS], (j / NS) & 1);
     for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j) mbar_wait_drain(&s.v_full[j % NS], (j / NS) & 1);
   } else if (warp == 1 && lane == 0) {
@@ -232,66 +202,45 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
       for (int ks = 0; ks < kTile / 16; ++ks)
         umma_ts(d, tbase + TM::kS(qi) + ks * 8, desc_at(dMN, va + ks * 2048), idPV, (acc || ks > 0) ? 1u : 0u);
     };
-    auto wait = [&](uint64_t* bar, uint32_t par) { return pipe_wait(bar, par, &s.abort_flag, vstatus); };
-    bool ok = true;
-    int T = 0, ku = 0;  // K/V tiles and units (with keys) issued by this CTA
-    for (int r = 0; ok; ++r) {
-      const int u = fwd_unit_of(r, blockIdx.x, gridDim.x, n_units);
-      if (u < 0) break;
-      const FwdUnit x = decode_fwd_unit(seg, g, u, NQ);
-      if (!x.ok || x.nk == 0) continue;
-      const int nk = x.nk;
-      // first S of the unit: each S buffer was last read by the previous
-      // unit's final PV product, issued before
-      if (!wait(&s.q_full, ku & 1) || !wait(&s.k_full[T % NS], (T / NS) & 1)) {
+    bool ok = pipe_wait(&s.q_full, 0, &s.abort_flag, vstatus) &&
+              pipe_wait(&s.k_full[0], 0, &s.abort_flag, vstatus);
+    if (ok) {
+      tc_fence_after();
+      for (int qi = 0; qi < NQ; ++qi) {
+        issue_s(qi, 0);
+        umma_commit(&s.s_full[qi]);
+      }
+      umma_commit(&s.k_empty[0]);
+    }
+    for (int j = 0; ok && j < nk; ++j) {
+      const int st = j % NS;
+      if (!pipe_wait(&s.v_full[st], (j / NS) & 1, &s.abort_flag, vstatus)) {
         ok = false;
         break;
       }
-      tc_fence_after();
       for (int qi = 0; qi < NQ; ++qi) {
-        issue_s(qi, T % NS);
-        umma_commit(&s.s_full[qi]);
-      }
-      umma_commit(&s.k_empty[T % NS]);
-      if (nk == 1) umma_commit(&s.q_empty);  // the unit's last S products read Q
-      for (int j = 0; j < nk; ++j, ++T) {
-        const int st = T % NS;
-        if (!wait(&s.v_full[st], (T / NS) & 1)) {
+        if (!pipe_wait(&s.p_full[qi], j & 1, &s.abort_flag, vstatus)) {
           ok = false;
           break;
         }
-        for (int qi = 0; qi < NQ; ++qi) {
-          if (!wait(&s.p_full[qi], T & 1)) {
-            ok = false;
-            break;
-          }
-          // the unit's first PV overwrites O: the previous unit's must be read out
-          if (j == 0 && ku > 0 && !wait(&s.o_free[qi], (ku - 1) & 1)) {
+        tc_fence_after();
+        issue_pv(qi, st, j > 0);
+        umma_commit(&s.o_done[qi]);
+        if (j + 1 < nk) {
+          const int st1 = (j + 1) % NS;
+          if (qi == 0 &&
+              !pipe_wait(&s.k_full[st1], ((j + 1) / NS) & 1, &s.abort_flag, vstatus)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(qi, st, j > 0);
-          umma_commit(&s.o_done[qi]);
-          if (j + 1 < nk) {
-            const int st1 = (T + 1) % NS;
-            if (qi == 0 && !wait(&s.k_full[st1], ((T + 1) / NS) & 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(qi, st1);
-            umma_commit(&s.s_full[qi]);
-          }
-        }
-        if (!ok) break;
-        umma_commit(&s.v_empty[st]);
-        if (j + 1 < nk) {
-          umma_commit(&s.k_empty[(T + 1) % NS]);
-          if (j + 2 == nk) umma_commit(&s.q_empty);  // the unit's last S products read Q
+          issue_s(qi, st1);
+          umma_commit(&s.s_full[qi]);
         }
       }
-      ++ku;
+      if (!ok) break;
+      umma_commit(&s.v_empty[st]);
+      if (j + 1 < nk) umma_commit(&s.k_empty[(j + 1) % NS]);
     }
     if (!ok) {
       s.abort_flag = 1;
@@ -306,152 +255,139 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t t_s = tbase + lane_off + TM::kS(qi);
     const uint32_t t_o = tbase + lane_off + TM::kO(qi);
+    const int h = h0 + qi;
+    const int i = qt * kTile + r;
+    const bool real = i < n_real;
+    int jlo = 1, jhi = 0;  // allowed K/V buffer rows [jlo, jhi] of this row
+    if (real) {
+      const int p = g.row_offset + i;
+      const int doc_start = seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i];
+      jlo = row_lo_window(doc_start, p, g.window) - g.kv_offset;
+      jhi = min(p - g.kv_offset, g.S_kv - 1);  // a K/V chunk may end before the row
+    }
     const float sl2 = g.scale * 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
-    int T = 0, ku = 0;  // K/V tiles and units (with keys) done by this CTA
-    for (int ru = 0; ok; ++ru) {
-      const int u = fwd_unit_of(ru, blockIdx.x, gridDim.x, n_units);
-      if (u < 0) break;
-      const FwdUnit x = decode_fwd_unit(seg, g, u, NQ);
-      if (!x.ok) continue;
-      const int b = x.b, nk = x.nk, kt_lo = x.kt_lo, n_real = x.n_real;
-      const int h = x.h0 + qi;
-      const int i = x.qt * kTile + r;
-      const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
-      if (nk == 0) {
-        // No row of this q tile sees a key: zeros and -inf (merging: a running
-        // result is kept, an empty one set to zeros and -inf).
-        if (i < g.L && (!kMerge || lse[row] == -INFINITY)) {
-          uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
-          for (int c = 0; c < D / 8; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-          lse[row] = -INFINITY;
-        }
-        continue;
+    for (int j = 0; j < nk; ++j) {
+      uint32_t km[4];  // dropout: keep bits of this row over the tile's 128 keys
+      if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
+      if (!warp_wait(&s.s_full[qi], j & 1, &s.abort_flag, vstatus)) {
+        ok = false;
+        break;
       }
-      const bool real = i < n_real;
-      int jlo = 1, jhi = 0;  // allowed K/V buffer rows [jlo, jhi] of this row
-      if (real) {
-        const int p = g.row_offset + i;
-        const int doc_start = seg[g.off[BD_SEG_OFF_ROW_LO] + b * g.L + i];
-        jlo = row_lo_window(doc_start, p, g.window) - g.kv_offset;
-        jhi = min(p - g.kv_offset, g.S_kv - 1);  // a K/V chunk may end before the row
+      tc_fence_after();
+      // S in two halves: the second half's load is in flight while the first
+      // half's max is formed
+      uint32_t xr[128];
+      tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
+      tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
+      tmem_wait_ld();
+      tmem_regs_ready<64>(&xr[0]);
+      tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&xr[64]));
+      tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
+      const int c0 = (kt_lo + j) * kTile;
+      // a row either sees the whole tile, none of it (another document, or a
+      // padding row), or part of it (the diagonal / document-start tiles); only
+      // a warp with a partly seen row needs the per-element mask
+      const bool dead = jhi < c0 || jlo > c0 + kTile - 1;
+      const bool unmasked = __all_sync(0xffffffffu, dead || (jlo <= c0 && c0 + kTile - 1 <= jhi));
+      const int a_lo = jlo - c0, e_hi = jhi - c0;
+      float x[128];  // raw scores, -inf where masked
+      float mx[8];   // eight independent 16-column maxima (short dependency chains)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        if (hf == 1) {
+          tmem_wait_ld();
+          tmem_regs_ready<64>(&xr[64]);
+        }
+        if (unmasked) {
+#pragma unroll
+          for (int c = 64 * hf; c < 64 * hf + 64; ++c) x[c] = __uint_as_float(xr[c]);
+        } else {
+#pragma unroll
+          for (int c = 64 * hf; c < 64 * hf + 64; ++c) x[c] = (c >= a_lo && c <= e_hi) ? __uint_as_float(xr[c]) : -INFINITY;
+        }
+#pragma unroll
+        for (int k = 4 * hf; k < 4 * hf + 4; ++k) {
+          float a = fmax3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+#pragma unroll
+          for (int c = 16 * k + 3; c < 16 * k + 15; c += 2) a = fmax3(a, x[c], x[c + 1]);
+          mx[k] = fmaxf(a, x[16 * k + 15]);
+        }
       }
-      float m = -INFINITY, l = 0.f;
-      for (int j = 0; j < nk; ++j, ++T) {
-        uint32_t km[4];  // dropout: keep bits of this row over the tile's 128 keys
-        if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
-        if (!warp_wait(&s.s_full[qi], T & 1, &s.abort_flag, vstatus)) {
-          ok = false;
-          break;
+      float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      tmax = dead ? -INFINITY : tmax * sl2;  // the scale is positive: the max of the scaled scores
+      const float m_new = fmaxf(m, tmax);
+      const bool need = m_new > m + 8.0f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? fast_exp2(m - m_new) : 1.0f;
+        if (need) {
+          l *= alpha;
+          m = m_new;
         }
-        tc_fence_after();
-        // S in two halves: the second half's load is in flight while the first
-        // half's max is formed
-        uint32_t xr[128];
-        tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
-        tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
-        tmem_wait_ld();
-        tmem_regs_ready<64>(&xr[0]);
-        tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&xr[64]));
-        tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&xr[96]));
-        const int c0 = (kt_lo + j) * kTile;
-        // a row either sees the whole tile, none of it (another document, or a
-        // padding row), or part of it (the diagonal / document-start tiles); only
-        // a warp with a partly seen row needs the per-element mask
-        const bool dead = jhi < c0 || jlo > c0 + kTile - 1;
-        const bool unmasked = __all_sync(0xffffffffu, dead || (jlo <= c0 && c0 + kTile - 1 <= jhi));
-        const int a_lo = jlo - c0, e_hi = jhi - c0;
-        float xs[128];  // raw scores, -inf where masked
-        float mx[8];    // eight independent 16-column maxima (short dependency chains)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          if (hf == 1) {
-            tmem_wait_ld();
-            tmem_regs_ready<64>(&xr[64]);
+        if (j > 0) {
+          if (!warp_wait(&s.o_done[qi], (j - 1) & 1, &s.abort_flag, vstatus)) {
+            ok = false;
+            break;
           }
-          if (unmasked) {
-#pragma unroll
-            for (int c = 64 * hf; c < 64 * hf + 64; ++c) xs[c] = __uint_as_float(xr[c]);
-          } else {
-#pragma unroll
-            for (int c = 64 * hf; c < 64 * hf + 64; ++c) xs[c] = (c >= a_lo && c <= e_hi) ? __uint_as_float(xr[c]) : -INFINITY;
-          }
-#pragma unroll
-          for (int k = 4 * hf; k < 4 * hf + 4; ++k) {
-            float a = fmax3(xs[16 * k], xs[16 * k + 1], xs[16 * k + 2]);
-#pragma unroll
-            for (int c = 16 * k + 3; c < 16 * k + 15; c += 2) a = fmax3(a, xs[c], xs[c + 1]);
-            mx[k] = fmaxf(a, xs[16 * k + 15]);
-          }
-        }
-        float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-        tmax = dead ? -INFINITY : tmax * sl2;  // the scale is positive: the max of the scaled scores
-        const float m_new = fmaxf(m, tmax);
-        const bool need = m_new > m + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2(m - m_new) : 1.0f;
-          if (need) {
-            l *= alpha;
-            m = m_new;
-          }
-          if (j > 0) {
-            if (!warp_wait(&s.o_done[qi], (T - 1) & 1, &s.abort_flag, vstatus)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-              uint32_t o[32];
-              tmem_ld32(t_o + c, o);
-              tmem_wait_ld();
-              const float2 av = make_float2(alpha, alpha);
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+            const float2 av = make_float2(alpha, alpha);
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), av);
-                o[e] = __float_as_uint(v.x);
-                o[e + 1] = __float_as_uint(v.y);
-              }
-              tmem_st32(t_o + c, o);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = __fmul2_rn(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), av);
+              o[e] = __float_as_uint(v.x);
+              o[e + 1] = __float_as_uint(v.y);
             }
-            tmem_wait_st();
+            tmem_st32(t_o + c, o);
           }
+          tmem_wait_st();
         }
-        // exponent offset; -inf on a row that sees nothing of this tile, so P = 0
-        const float nmm = dead ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
-        // two-wide fp32 FMA and add (one instruction per pair of columns): the
-        // exponent scale * log2(e) * score - max, and the row sum in four pairs
-        // of partial sums
-        const float2 sl2v = make_float2(sl2, sl2), nmmv = make_float2(nmm, nmm);
-        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float2 ex = __ffma2_rn(make_float2(xs[2 * c], xs[2 * c + 1]), sl2v, nmmv);
-          const float p0 = fast_exp2(ex.x), p1 = fast_exp2(ex.y);
-          rs2[c & 3] = __fadd2_rn(rs2[c & 3], make_float2(p0, p1));
-          if constexpr (kDrop) {
-            const uint32_t kb = km[c >> 4] >> ((2 * c) & 31);
-            pk[c] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
-          } else {
-            pk[c] = pack_bf16x2(p0, p1);
-          }
-        }
-        const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
-        const float2 rsum = __fadd2_rn(r01, r23);
-        l += rsum.x + rsum.y;
-        tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.p_full[qi]);
       }
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok && !warp_wait(&s.o_done[qi], (T - 1) & 1, &s.abort_flag, vstatus)) ok = false;
-      if (!ok) break;
+      // exponent offset; -inf on a row that sees nothing of this tile, so P = 0
+      const float nmm = dead ? -INFINITY : (m == -INFINITY) ? 0.f : -m;
+      // two-wide fp32 FMA and add (one instruction per pair of columns): the
+      // exponent scale * log2(e) * score - max, and the row sum in four pairs
+      // of partial sums
+      const float2 sl2v = make_float2(sl2, sl2), nmmv = make_float2(nmm, nmm);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float2 ex = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), sl2v, nmmv);
+        const float p0 = fast_exp2(ex.x), p1 = fast_exp2(ex.y);
+        rs2[c & 3] = __fadd2_rn(rs2[c & 3], make_float2(p0, p1));
+        if constexpr (kDrop) {
+          const uint32_t kb = km[c >> 4] >> ((2 * c) & 31);
+          pk[c] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
+        } else {
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+      }
+      const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
+      const float2 r = __fadd2_rn(r01, r23);
+      const float rs = r.x + r.y;
+      l += rs;
+      tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.p_full[qi]);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !warp_wait(&s.o_done[qi], (nk - 1) & 1, &s.abort_flag, vstatus)) ok = false;
+    if (!ok) {
+      s.abort_flag = 1;
+      if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
+    } else {
       tc_fence_after();
       float inv = l > 0.f ? (kDrop ? g.drop_scale : 1.0f) / l : 0.f;
       float lse_v = (real && l > 0.f) ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const size_t row = (static_cast<size_t>(b) * g.Hq + h) * g.L + i;
       uint4* o4 = reinterpret_cast<uint4*>(out + row * D);
       // merging into a running (out, lse): log-sum-exp weights of the two sides;
       // an empty side (lse -inf) has weight 0 and its out is not read
@@ -462,11 +398,11 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         if (lse_v == -INFINITY) {
           store = lse_o == -INFINITY;  // nothing new: keep a running result, zero an empty one
         } else if (lse_o != -INFINITY) {
-          const float mxl = fmaxf(lse_o, lse_v);
-          const float ea = expf(lse_o - mxl), eb = expf(lse_v - mxl), tot = ea + eb;
+          const float mx = fmaxf(lse_o, lse_v);
+          const float ea = expf(lse_o - mx), eb = expf(lse_v - mx), tot = ea + eb;
           w_old = ea / tot;
           inv *= eb / tot;
-          lse_v = mxl + logf(tot);
+          lse_v = mx + logf(tot);
         }
       }
 #pragma unroll 1
@@ -500,14 +436,6 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         }
       }
       if (store) lse[row] = lse_v;
-      // O has been read: the next unit's first PV product may overwrite it
-      tc_fence_before();
-      mbar_arrive(&s.o_free[qi]);
-      ++ku;
-    }
-    if (!ok) {
-      s.abort_flag = 1;
-      if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
   }
 
@@ -528,15 +456,8 @@ static cudaError_t launch_one(const CUtensorMap& mq, const CUtensorMap& mk, cons
                        : (merge ? fwd_kernel<D, NQ, NS, true, false> : fwd_kernel<D, NQ, NS, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  // persistent: one CTA per SM at most (tensor memory allows one)
-  int dev = 0, n_sm = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  const long long units = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);
-  const long long grid = units < n_sm ? units : n_sm;
-  if (grid <= 0 || units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long grid = static_cast<long long>(g.B) * g.nqt * (g.Hq / NQ);
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(128 + NQ * 128), smem, st, mq,
       mk, mv, seg, g, out, lse, status); le != cudaSuccess) return le;
   return cudaGetLastError();
