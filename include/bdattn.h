@@ -86,10 +86,10 @@ typedef struct {
  * key s taking draw s mod 8 (word (s mod 8) / 2; low half for even s); the pair
  * is kept iff its draw u >= T = round(dropout_p * 2^16). Decisions depend on
  * global positions only, so K/V chunks, shards and buffer offsets agree.
- * Dropout is built for D = 64, 128 and 256: every forward and backward entry
- * point returns BD_ERR_ARG for dropout_p > 0 at D = 512, and for dropout_p
- * outside [0, 1) or rounding to T = 2^16. A forward and the backward of the
- * same step must use the same dropout_p and seed. */
+ * Every forward and backward entry point takes dropout, at every head dim;
+ * they return BD_ERR_ARG for dropout_p outside [0, 1) or rounding to
+ * T = 2^16. A forward and the backward of the same step must use the same
+ * dropout_p and seed. */
 
 /* K/V layouts. BD_KV_SBHD is token-major, [S_kv][B][Hkv][D]: the receive
  * buffer of the needed-only all-to-all-v (pieces in source order make the

@@ -295,7 +295,6 @@ int fwd_impl(const void* q, const void* k, const void* v, const void* seg, const
              int32_t* status, int merge, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   if (!q || !k || !v || !seg || !out || !lse || !status) return BD_ERR_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(seg)) return BD_ERR_ARG;
   if (int rc = check_device()) return rc;
@@ -331,7 +330,6 @@ int bwd_prep_impl(const void* dout, const void* out, const bd_geom* gi, void* wo
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   if (!dout || !out || !workspace || !status) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
   if (dq_f32 && !aligned16(dq_f32)) return BD_ERR_ARG;
@@ -344,7 +342,6 @@ int bwd_main_impl(const void* dout, const void* q, const void* k, const void* v,
                   int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   if (!dout || !q || !k || !v || !lse || !seg || !dk || !dv || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv) ||
@@ -395,7 +392,6 @@ int bd_attn_bwd_finalize(const bd_geom* gi, int grad_dtype, void* dq, void* work
                          bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   if (!dq || !workspace || !status) return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
   if (!aligned16(dq) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return BD_ERR_ARG;
@@ -409,7 +405,6 @@ int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, co
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;
   if (grad_dtype != BD_DTYPE_F32 && grad_dtype != BD_DTYPE_BF16) return BD_ERR_ARG;
@@ -439,7 +434,6 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
                 int32_t* status, bd_stream_t stream) {
   Geom g;
   if (int rc = to_geom(gi, &g)) return rc;
-  if (g.drop_t && g.D == 512) return BD_ERR_ARG;  // dropout is built for D <= 256
   // check everything up front so that a bad argument enqueues nothing
   if (!dout || !q || !k || !v || !out || !lse || !seg || !dq || !dk || !dv || !workspace || !status)
     return BD_ERR_ARG;

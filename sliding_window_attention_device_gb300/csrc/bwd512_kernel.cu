@@ -26,10 +26,14 @@
 //   warps 8-11  dQ read-out (thread = d row of the slice), red.global.add
 // The tensor pipe runs 22 D FLOPs per allowed (row, key) pair against the
 // 10 D counted: S^T and dP^T are formed once per slice.
+// With attention dropout (kDrop) each P / dS warp draws its 32 keys' keep
+// masks over the half's q columns (dropout.cuh): dropped weights are zeroed in
+// P^T, dS = P (Z dP - delta), and dV is scaled by the keep scale when written.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -76,7 +80,7 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 __device__ __forceinline__ int streamed_chunk(int c, int i) { return i < 2 * c ? i : i + 2; }
 
 // kDq: with the dq products (else dK / dV only, for the fixed-order dq pass).
-template <bool kDq>
+template <bool kDq, bool kDrop>
 __global__ void __launch_bounds__(kThreads5, 1)
     bwd512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -379,11 +383,16 @@ __global__ void __launch_bounds__(kThreads5, 1)
       }
     }
     const int row_end = min(doc_end, g.window > 0 ? key + g.window : 0x3fffffff);
+    // dropout: scale * keep scale multiplies a kept dP (a dropped one is zero)
+    const float sc_dp = kDrop ? g.scale * g.drop_scale : g.scale;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int st = it & 1;  // slot of this tile's row values
       int h, q0;
       decode(it, h, q0);
+      uint64_t km = 0;  // dropout: keep bits of this key over the half's 32 q columns
+      if constexpr (kDrop)
+        km = key_keep_mask<4>(g, b, h, g.row_offset + q0 + c0, g.kv_offset + kt * kTile + (warp & 3) * 32, lane);
       // the slice stage's barrier also publishes this tile's row values
       if (!warp_wait(&s.qs_full, it & 1, &s.abort_flag, vstatus) ||
           !warp_wait(&s.s_full, it & 1, &s.abort_flag, vstatus)) {
@@ -413,7 +422,12 @@ __global__ void __launch_bounds__(kThreads5, 1)
       }
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      for (int c = 0; c < 16; ++c) {
+        if constexpr (kDrop)
+          pk[c] = pack_bf16x2(((km >> (2 * c)) & 1u) ? p[2 * c] : 0.f, ((km >> (2 * c + 1)) & 1u) ? p[2 * c + 1] : 0.f);
+        else
+          pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+      }
       tmem_st16(tbase + lane_off + kColS + 48 * half, pk);
       tmem_wait_st();
       tc_fence_before();
@@ -431,10 +445,14 @@ __global__ void __launch_bounds__(kThreads5, 1)
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 dl = d4[c4];
         const int c = 4 * c4;
-        pk[2 * c4] = pack_bf16x2(p[c] * fmaf(__uint_as_float(sr[c]), g.scale, -dl.x),
-                                 p[c + 1] * fmaf(__uint_as_float(sr[c + 1]), g.scale, -dl.y));
-        pk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(__uint_as_float(sr[c + 2]), g.scale, -dl.z),
-                                     p[c + 3] * fmaf(__uint_as_float(sr[c + 3]), g.scale, -dl.w));
+        float dp[4] = {__uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), __uint_as_float(sr[c + 2]),
+                       __uint_as_float(sr[c + 3])};
+        if constexpr (kDrop) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dp[e] = ((km >> (c + e)) & 1u) ? dp[e] : 0.f;
+        }
+        pk[2 * c4] = pack_bf16x2(p[c] * fmaf(dp[0], sc_dp, -dl.x), p[c + 1] * fmaf(dp[1], sc_dp, -dl.y));
+        pk[2 * c4 + 1] = pack_bf16x2(p[c + 2] * fmaf(dp[2], sc_dp, -dl.z), p[c + 3] * fmaf(dp[3], sc_dp, -dl.w));
       }
       if (it > 0 && !warp_wait(&s.ds_empty, (it - 1) & 1, &s.abort_flag, vstatus)) {
         ok = false;
@@ -462,6 +480,10 @@ __global__ void __launch_bounds__(kThreads5, 1)
           uint32_t vv[32];
           tmem_ld32(tbase + lane_off + kColDv + c, vv);
           tmem_wait_ld();
+          if constexpr (kDrop) {  // dropout: the keep scale of P^T
+#pragma unroll
+            for (int e = 0; e < 32; ++e) vv[e] = __float_as_uint(__uint_as_float(vv[e]) * g.drop_scale);
+          }
           uint32_t kk[32];
           tmem_ld32(tbase + lane_off + kColDk + c, kk);
           tmem_wait_ld();
@@ -555,7 +577,8 @@ cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, co
                                cudaStream_t st) {
   if (g.D != kD5) return cudaErrorInvalidValue;
   const size_t smem = sizeof(Bwd512Smem) + 1024;  // + 1 KB to align the swizzled tiles
-  auto kern = dq_acc ? bwd512_kernel<true> : bwd512_kernel<false>;
+  auto kern = g.drop_t ? (dq_acc ? bwd512_kernel<true, true> : bwd512_kernel<false, true>)
+                       : (dq_acc ? bwd512_kernel<true, false> : bwd512_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int reach = kv_tiles_reachable(g);

@@ -15,6 +15,8 @@
 // never overwrites a dS they still read.
 //   warp 0   TMA: Q and dO once, the chunk ring     warp 1  one thread issues the MMAs
 //   warp 2   tensor memory                          warps 4-7  thread = q row: P, dS, dq rows
+// With attention dropout (kDrop) each row draws its keep mask of a K/V tile
+// (dropout.cuh) before the tile's S and dP arrive: dS = P (Z dP - delta).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>

@@ -12,11 +12,14 @@
 // for S, (dO, V) pairs for dP, then this half's K chunks for dQ.
 //   warp 0   TMA: the chunk ring      warp 1  one thread issues the MMAs
 //   warp 2   tensor memory            warps 4-7  thread = q row: P, dS, dq rows
+// With attention dropout (kDrop) each row draws its keep mask of a K/V tile
+// (dropout.cuh) before the tile's S and dP arrive: dS = P (Z dP - delta).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
 #include "dq_stream.cuh"
+#include "dropout.cuh"
 
 namespace bd {
 
@@ -49,6 +52,7 @@ struct Dq512Smem {
 };
 static_assert(sizeof(Dq512Smem) + 1024 <= 232448, "shared memory per CTA");
 
+template <bool kDrop>
 __global__ void __launch_bounds__(kThreads5, 1)
     bwd_dq512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dout,
                      const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -243,6 +247,8 @@ __global__ void __launch_bounds__(kThreads5, 1)
     }
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
+      uint32_t km[4] = {0u, 0u, 0u, 0u};  // dropout: keep bits of this row over the tile's 128 keys
+      if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
       if (!warp_wait(&s.sdp_full, j & 1, &s.abort_flag, vstatus)) {
         ok = false;
         break;
@@ -253,8 +259,8 @@ __global__ void __launch_bounds__(kThreads5, 1)
       const bool dead = !real || jhi < c0 || jlo > c0 + kTile - 1;
       const bool full = jlo <= c0 && c0 + kTile - 1 <= jhi;
       uint32_t pk[2][32];  // dS of keys [64 hf, 64 hf + 64), bf16 pairs
-      dq_form_ds(tbase + lane_off + kColS, tbase + lane_off + kColDp, g.scale, nl2, ndl, dead, full, jlo - c0,
-                 jhi - c0, pk);
+      dq_form_ds<kDrop>(tbase + lane_off + kColS, tbase + lane_off + kColDp, g.scale, nl2, ndl, dead, full, jlo - c0,
+                        jhi - c0, pk, km, g.drop_scale);
       // dS over this row's S columns (read above): the A operand of the dQ products
       tmem_st32(tbase + lane_off + kColS, pk[0]);
       tmem_st32(tbase + lane_off + kColS + 32, pk[1]);
@@ -296,11 +302,12 @@ cudaError_t launch_bwd_dq512(const CUtensorMap& mq, const CUtensorMap& mdo, cons
   e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(bwd_dq512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kern = g.drop_t ? bwd_dq512_kernel<true> : bwd_dq512_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * g.Hq * 2;  // (q tile, query head, half)
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (const cudaError_t le = launch_pdl(bwd_dq512_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads5), smem,
+  if (const cudaError_t le = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads5), smem,
       st, mq, mdo, mk, mv, seg, g, lse, delta, dq, bf16, status); le != cudaSuccess) return le;
   return cudaGetLastError();
 }

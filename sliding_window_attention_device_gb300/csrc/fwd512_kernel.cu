@@ -15,10 +15,15 @@
 //            a V half per tile
 //   warp 1   one thread issues the MMAs      warp 2  tensor memory
 //   warps 4-7  thread = q row: softmax, P (bf16 over S in tensor memory), out
+// With attention dropout (kDrop) each row draws its keep mask of a tile (in
+// both passes) before the tile's S arrives, zeroes the dropped weights of the
+// P it hands to the PV products (the row sum stays the undropped one) and
+// folds the keep scale into the scale of each O half.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "dropout.cuh"
 #include "pipeline.cuh"
 
 namespace bd {
@@ -49,7 +54,7 @@ struct Fwd512Smem {
 
 // kMerge: merge this K/V chunk's result into the running (out, lse) instead
 // of writing it (log-sum-exp weights, as the merge kernel).
-template <bool kMerge>
+template <bool kMerge, bool kDrop>
 __global__ void __launch_bounds__(kThreads512, 1)
     fwd512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ seg, const Geom g,
@@ -256,6 +261,8 @@ __global__ void __launch_bounds__(kThreads512, 1)
     int t = 0;
     for (int p = 0; p < 2 && ok; ++p) {
       for (int j = 0; j < nk; ++j, ++t) {
+        uint32_t km[4];  // dropout: keep bits of this row over the tile's 128 keys
+        if constexpr (kDrop) row_keep_mask(g, b, h, g.row_offset + i, g.kv_offset + (kt_lo + j) * kTile, km);
         if (!warp_wait(&s.s_full[t & 1], (t >> 1) & 1, &s.abort_flag, vstatus)) {
           ok = false;
           break;
@@ -333,7 +340,12 @@ __global__ void __launch_bounds__(kThreads512, 1)
             p1 = (2 * c + 1 >= a_lo && 2 * c + 1 <= e_hi) ? p1 : 0.f;
           }
           rs2 = __fadd2_rn(rs2, make_float2(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
+          if constexpr (kDrop) {
+            const uint32_t kb = km[c >> 4] >> ((2 * c) & 31);
+            pk[c] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
+          } else {
+            pk[c] = pack_bf16x2(p0, p1);
+          }
         }
         if (p == 0) l += rs2.x + rs2.y;
         tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(pk));
@@ -348,7 +360,8 @@ __global__ void __launch_bounds__(kThreads512, 1)
       if (ok && !warp_wait(&s.o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, &s.abort_flag, vstatus)) ok = false;
       if (!ok) break;
       tc_fence_after();
-      float scale_o = w_new;  // pass 1: P was already normalised
+      const float dscale = kDrop ? g.drop_scale : 1.0f;  // dropout: the keep scale of P
+      float scale_o = w_new * dscale;  // pass 1: P was already normalised
       if (p == 0) {
         empty = !(real && l > 0.f);
         float lse_v = empty ? -INFINITY : (m + __log2f(l)) * 0.6931471805599453f;
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kThreads512, 1)
           }
         }
         if (store) lse[row] = lse_v;
-        scale_o = empty ? 0.f : w_new / l;
+        scale_o = empty ? 0.f : w_new * dscale / l;
       }
       uint4* o4 = reinterpret_cast<uint4*>(out + row * kD512 + 256 * p);
 #pragma unroll 1
@@ -429,7 +442,8 @@ cudaError_t launch_fwd512(const CUtensorMap& mq, const CUtensorMap& mk, const CU
   e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   if (smem > static_cast<size_t>(max_optin)) return cudaErrorInvalidValue;
-  auto kern = merge ? fwd512_kernel<true> : fwd512_kernel<false>;
+  auto kern = g.drop_t ? (merge ? fwd512_kernel<true, true> : fwd512_kernel<false, true>)
+                       : (merge ? fwd512_kernel<true, false> : fwd512_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(g.B) * g.nqt * g.Hq;  // (q tile, query head)

@@ -145,8 +145,8 @@ def test_deterministic_backward_rejects_null_pointers(lib):
 
 
 def test_dropout_arguments_are_checked_on_the_host():
-    """dropout_p outside [0, 1), or rounding to a threshold of 2^16, and any
-    dropout at head dim 512 are refused before anything touches a device."""
+    """dropout_p outside [0, 1), or rounding to a threshold of 2^16, is refused
+    before anything touches a device."""
     lib = bdattn.load()
     P = ctypes.c_void_p
     for p in (1.0, -0.1, float("nan"), 0.99999999):
@@ -154,10 +154,6 @@ def test_dropout_arguments_are_checked_on_the_host():
         assert lib.bd_attn_fwd(P(16), P(16), P(16), P(16), ctypes.byref(g), P(16), P(16), P(16), None) == \
             bdattn.BD_ERR_ARG, p
         assert lib.bd_attn_seg_bytes(ctypes.byref(g)) == 0
-    g = bdattn.geom(1, 2, 1, 512, 1024, 256, 256, 0, 1024, dropout_p=0.1, seed=3)
-    assert lib.bd_attn_fwd(P(16), P(16), P(16), P(16), ctypes.byref(g), P(16), P(16), P(16), None) == \
-        bdattn.BD_ERR_ARG
-    assert lib.bd_attn_bwd(P(16), P(16), P(16), P(16), P(16), P(16), P(16), ctypes.byref(g), 0, P(16), P(16), P(16),
-                           P(256), P(16), None) == bdattn.BD_ERR_ARG
-    assert lib.bd_attn_bwd_deterministic(P(16), P(16), P(16), P(16), P(16), P(16), P(16), ctypes.byref(g), 0,
-                                         P(16), P(16), P(16), P(256), P(16), None) == bdattn.BD_ERR_ARG
+    for D in (64, 128, 256, 512):  # a valid probability passes the host checks at every head dim
+        g = bdattn.geom(1, 2, 1, D, 1024, 256, 256, 0, 1024, dropout_p=0.1, seed=3)
+        assert lib.bd_attn_seg_bytes(ctypes.byref(g)) > 0

@@ -5,11 +5,11 @@ an attention weight is dropped. Both sides draw the keep decision of every (quer
 query position, key position) pair from Philox-4x32-10 with the counter
 (key / 8, query, head, batch row) and the seed, each from its own code; so
 out, lse, dq, dk and dv must agree within the parity bar for the same p and
-seed, as without dropout. The cases cover head dims 64 / 128 / 256, K/V
+seed, as without dropout. The cases cover head dims 64 / 128 / 256 / 512, K/V
 buffers that start at a position that is not a multiple of 8 (the decisions
 follow global positions), windows, GQA groups of 1 to 4, both gradient dtypes,
 the fixed-order (deterministic) backward, and K/V in chunks merged in the
-forward's epilogue.
+forward's epilogue, at head dims 64 to 512.
 
 Tolerance: the parity bar times the keep scale 2^16 / (2^16 - T). Every term
 a dropout run adds is an undropped term times Z <= that scale, and the terms
@@ -40,6 +40,8 @@ CASES = [
     ("d64_g1_window", W("c", 1, 3, 3, 64, 1024, 2, ("uniform", 50, 400, 70), window=100), 1),
     ("d256_g2_window", W("d", 1, 4, 2, 256, 1280, 4, ("uniform", 100, 600, 30), window=150, kv="prefix"), 3),
     ("d256_g1_needed", W("e", 2, 2, 2, 256, 1024, 4, ("uniform", 37, 501, 0), kv="needed"), 2),
+    ("d512_g2_needed", W("k", 1, 4, 2, 512, 1024, 4, ("uniform", 37, 501, 0), kv="needed"), 3),
+    ("d512_g1_window", W("l", 1, 2, 2, 512, 1024, 2, ("uniform", 40, 300, 10), window=90), 1),
 ]
 
 
@@ -91,7 +93,7 @@ def test_dropout_changes_the_result_and_follows_the_seed():
     assert torch.equal(a["lse"], base["lse"])  # the normaliser is the undropped softmax's
 
 
-@pytest.mark.parametrize("name", ["d128_g4_needed", "d256_g2_window"])
+@pytest.mark.parametrize("name", ["d128_g4_needed", "d256_g2_window", "d512_g2_needed"])
 def test_dropout_deterministic_backward(name):
     w, r = next((c[1], c[2]) for c in CASES if c[0] == name)
     c = _case(w, r, 0.3, 99)
@@ -113,10 +115,11 @@ def test_dropout_deterministic_backward(name):
     assert torch.equal(got[0][1], res["dk"]) and torch.equal(got[0][2], res["dv"])
 
 
-def test_dropout_chunked_forward_merge():
+@pytest.mark.parametrize("D", [128, 512])
+def test_dropout_chunked_forward_merge(D):
     """K/V in three chunks, each merged into the running (out, lse) in the
     forward's epilogue, equals the oracle's one-piece dropout forward."""
-    w = W("f", 1, 4, 2, 128, 1536, 4, ("uniform", 40, 900, 20))
+    w = W("f", 1, 4, 2, D, 1536, 4, ("uniform", 40, 900, 20))
     r = 3
     c = _case(w, r, 0.25, 1234)
     g = oracle_geom(c)
