@@ -783,10 +783,6 @@ cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, co
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
                                cudaStream_t st);
-cudaError_t launch_bwd256c_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
-                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
-                                const float* delta, float* dq_acc, void* dk, void* dv, int bf16, int32_t* status,
-                                cudaStream_t st);
 
 // Rows of the q / dout TMA boxes the backward main kernel for this head dim expects.
 int bwd_q_box_rows(int D) { return D <= 128 ? 128 : kBwdQ; }
@@ -812,8 +808,8 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
     case 64:
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
       return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
-    case 256:  // a cluster of two CTAs per K/V tile, one per half of the head dim (bwd256c_kernel.cu)
-      return launch_bwd256c_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
+    case 256:
+      return launch_main_d<256, true>(mq, mdo, mk, mv, mdq, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     case 512:  // the head dim of the outputs split over four CTAs (bwd512_kernel.cu)
       return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, delta, dq_acc, dk, dv, bf16, status, st);
     default: return cudaErrorInvalidValue;
@@ -834,9 +830,9 @@ cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, 
   if (g.D == 512)
     return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
                               st);
-  if (g.D == 256)
-    return launch_bwd256c_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
-                               st);
+  if (g.D == 256)  // the dq map is not read without the dq products
+    return launch_main_d<256, false>(mq, mdo, mk, mv, mq, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16,
+                                     status, st);
   return launch_bwd128_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
                             st);
 }
