@@ -8,8 +8,9 @@ out, lse, dq, dk and dv must agree within the parity bar for the same p and
 seed, as without dropout. The cases cover head dims 64 / 128 / 256 / 512, K/V
 buffers that start at a position that is not a multiple of 8 (the decisions
 follow global positions), windows, GQA groups of 1 to 4, both gradient dtypes,
-the fixed-order (deterministic) backward, and K/V in chunks merged in the
-forward's epilogue, at head dims 64 to 512.
+the fixed-order (deterministic) backward, K/V in chunks (forwards merged in
+the forward's epilogue, the per-chunk backward with the merged out / lse) at
+head dims 64 to 512, and token-major K/V read in place.
 
 Tolerance: the parity bar times the keep scale 2^16 / (2^16 - T). Every term
 a dropout run adds is an undropped term times Z <= that scale, and the terms
@@ -144,3 +145,102 @@ def test_dropout_chunked_forward_merge(D):
     assert int(status.item()) == 0
     assert_close("chunked dropout out", out, out_ref, *_bar(0.25))
     assert_lse(lse, lse_ref, real_rows(c))
+
+
+@pytest.mark.parametrize("D,window", [(64, 200), (128, 0), (256, 0), (512, 150)])
+def test_dropout_chunked_backward(D, window):
+    """The backward over K/V in three chunks (a ring step): per-chunk forwards
+    merged in the forward's epilogue, prep once with the merged out, one
+    backward main per chunk (dq accumulating, dk / dv per chunk), finalize --
+    equals the oracle's one-piece dropout backward. The chunks start off the
+    8-key grid of the draws, so each one's decisions come from global key
+    positions."""
+    w = W("g", 1, 4, 2, D, 1536, 4, ("uniform", 40, 900, 20), window=window)
+    r, p, seed = 3, 0.2, 0xC0FFEE
+    c = _case(w, r, p, seed)
+    g_ref = oracle_geom(c)
+    out_ref, lse_ref = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], g_ref)
+    dq_ref, dk_ref, dv_ref = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], g_ref)
+    dev = torch.device("cuda")
+    doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
+    q, do = c["q"].to(dev), c["do"].to(dev)
+    status = bdattn.new_status(dev)
+    out = torch.empty(w.B, w.Hq, w.L, w.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(w.B, w.Hq, w.L, dtype=torch.float32, device=dev)
+    cuts = (0, 301, 777, w.S)
+    chunks = []
+    for n in range(3):
+        a, e = cuts[n], cuts[n + 1]
+        gc = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, r * w.L, a, e - a, window, dropout_p=p, seed=seed)
+        segc, _ = bdattn.bd_attn_seg_build_chunk(doc, gc, status=status)
+        kc, vc = c["k"][:, :, a:e].contiguous().to(dev), c["v"][:, :, a:e].contiguous().to(dev)
+        if n == 0:
+            bdattn.bd_attn_fwd(q, kc, vc, segc, gc, status, out=out, lse=lse)
+        else:
+            bdattn.bd_attn_fwd_merge(q, kc, vc, segc, gc, status, out, lse)
+        chunks.append((gc, segc, kc, vc))
+    g_full = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, r * w.L, 0, w.S, window, dropout_p=p, seed=seed)
+    ws = torch.empty(bdattn.bwd_workspace_bytes(g_full), dtype=torch.uint8, device=dev)
+    dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.float32, device=dev)
+    bdattn.bd_attn_bwd_prep(do, out, g_full, status, ws)
+    dks, dvs = [], []
+    for gc, segc, kc, vc in chunks:
+        dk = torch.full((w.B, w.Hkv, gc.S_kv, w.D), float("nan"), dtype=torch.float32, device=dev)
+        dv = torch.full_like(dk, float("nan"))
+        bdattn.bd_attn_bwd_main(do, q, kc, vc, lse, segc, gc, status, ws, dk, dv)
+        dks.append(dk)
+        dvs.append(dv)
+    bdattn.bd_attn_bwd_finalize(g_full, status, ws, dq)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    mx, mn = _bar(p)
+    assert_close(f"D{D} chunked dropout out", out, out_ref, mx, mn)
+    assert_lse(lse, lse_ref, real_rows(c))
+    assert_close(f"D{D} chunked dropout dq", dq, dq_ref, mx, mn)
+    assert_close(f"D{D} chunked dropout dk", torch.cat(dks, dim=2), dk_ref, mx, mn)
+    assert_close(f"D{D} chunked dropout dv", torch.cat(dvs, dim=2), dv_ref, mx, mn)
+
+
+def _run_layout(c, layout):
+    """Forward and backward with K/V (and dK / dV) in the given layout; the
+    gradients come back head-major."""
+    w, dev = c["w"], torch.device("cuda")
+    g = bdattn.geom(w.B, w.Hq, w.Hkv, w.D, w.S, w.L, c["row_offset"], c["kv_offset"], c["S_kv"], w.window,
+                    kv_layout=layout, dropout_p=c["dropout_p"], seed=c["drop_seed"])
+    tm = layout == bdattn.KV_SBHD
+    to = (lambda t: t.permute(2, 0, 1, 3).contiguous()) if tm else (lambda t: t)
+    doc = torch.from_numpy(np.ascontiguousarray(c["doc"])).to(dev)
+    q, do = c["q"].to(dev), c["do"].to(dev)
+    k, v = to(c["k"]).to(dev), to(c["v"]).to(dev)
+    seg, status = bdattn.bd_attn_seg_build(doc, g)
+    out, lse = bdattn.bd_attn_fwd(q, k, v, seg, g, status)
+    dq = torch.full((w.B, w.Hq, w.L, w.D), float("nan"), dtype=torch.float32, device=dev)
+    dk = torch.full(bdattn.kv_shape(g), float("nan"), dtype=torch.float32, device=dev)
+    dv = torch.full_like(dk, float("nan"))
+    bdattn.bd_attn_bwd(do, q, k, v, out, lse, seg, g, status, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    back = (lambda t: t.permute(1, 2, 0, 3)) if tm else (lambda t: t)
+    return dict(out=out.cpu(), lse=lse.cpu(), dq=dq.cpu(), dk=back(dk).cpu(), dv=back(dv).cpu())
+
+
+@pytest.mark.parametrize("name", ["d128_g4_needed", "d256_g1_needed", "d512_g2_needed", "d64_g1_window"])
+def test_dropout_token_major(name):
+    """Token-major K/V (the receive buffer of the needed-only exchange, read in
+    place) under dropout: out, lse, dk and dv bit-equal to the head-major run,
+    and every output within the dropout bar of the oracle."""
+    w, r = next((x[1], x[2]) for x in CASES if x[0] == name)
+    c = _case(w, r, 0.3, 0xABCDEF0123)
+    a = _run_layout(c, bdattn.KV_BHSD)
+    t = _run_layout(c, bdattn.KV_SBHD)
+    assert torch.equal(a["out"], t["out"]) and torch.equal(a["lse"], t["lse"])
+    assert torch.equal(a["dk"], t["dk"]) and torch.equal(a["dv"], t["dv"])
+    g = oracle_geom(c)
+    out, lse = oracle.fwd(c["q"], c["k"], c["v"], c["doc"], g)
+    dq, dk, dv = oracle.bwd(c["q"], c["k"], c["v"], c["do"], c["doc"], g)
+    mx, mn = _bar(0.3)
+    assert_close(f"{name} token-major dropout out", t["out"], out, mx, mn)
+    assert_lse(t["lse"], lse, real_rows(c))
+    assert_close(f"{name} token-major dropout dq", t["dq"], dq, mx, mn)
+    assert_close(f"{name} token-major dropout dk", t["dk"], dk, mx, mn)
+    assert_close(f"{name} token-major dropout dv", t["dv"], dv, mx, mn)
