@@ -636,7 +636,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     e2e = None
     if not args.no_e2e and not chunked and not fwd_only:
-        e2e = run_e2e(rep, args, total_flop, world)
+        e2e = run_e2e(rep, args, total_flop, world, ms_per_step)
 
     if rank != 0:
         return None
@@ -716,7 +716,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     return line
 
 
-def run_e2e(rep: Replica, args, total_flop: float, world: int) -> dict:
+def run_e2e(rep: Replica, args, total_flop: float, world: int, device_ms: float) -> dict:
     """Same step through the C ABI with host buffers: pinned host inputs copied in
     and every output copied back inside the timed region. As a user would run it,
     the copies overlap the kernels: one stream brings each shard's inputs in ahead
@@ -789,9 +789,29 @@ def run_e2e(rep: Replica, args, total_flop: float, world: int) -> dict:
     if int(rep.status.item()) != 0:
         raise RuntimeError(f"device status {int(rep.status.item()):#x} in the end-to-end run")
     ms = allreduce_max(t0.elapsed_time(t1) / steps, dev, world)
+    # the host link on its own, after the timed region: the largest output copied
+    # out and the largest input copied in, three times each
+    def link_gbs(dst, src, stream):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)  # warm-up
+            a.record(stream)
+            for _ in range(3):
+                dst.copy_(src, non_blocking=True)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return 3 * src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+    big = max(((h_out[i][nm], s[nm]) for i, s in enumerate(rep.shards) for nm in h_out[i]),
+              key=lambda p: p[1].numel() * p[1].element_size())
+    bw_d2h = link_gbs(big[0], big[1], s_out)
+    bw_h2d = link_gbs(rep.k_full, h_k, s_in)
+    bound = max(device_ms, h2d / (bw_h2d * 1e9) * 1e3, d2h / (bw_d2h * 1e9) * 1e3)
     return {"value": round(job_tflops(total_flop, ms, world), 2), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "copies": "pinned host buffers, overlapped with the kernels on two copy streams"}
+            "copies": "pinned host buffers, overlapped with the kernels on two copy streams",
+            "link_gbs": {"h2d": round(bw_h2d, 1), "d2h": round(bw_d2h, 1)},
+            "bound_ms": round(bound, 3), "frac_of_bound": round(bound / ms, 4),
+            "bound_note": "max of the device step and each direction's bytes over its measured link rate"}
 
 
 # ------------------------------------------------------------ CPU oracle
