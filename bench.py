@@ -59,7 +59,7 @@ BWD_KERNEL = {64: "bwd128_kernel<64>", 128: "bwd128_kernel<128>", 256: "bwd_kern
               512: "bwd512_kernel (four CTAs per K/V tile, one per 128-column slice)"}
 # the fixed-order dq pass of each head dim above 128
 DQ_KERNEL = {256: "bwd_dq256_kernel", 512: "bwd_dq512_kernel (two CTAs per q tile, one per 256-column half)"}
-TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "cd9d083444a3a85a", "bytes_per_launch": 1.16909e9}
+TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "d43094137af5baa5", "bytes_per_launch": 1.19089e9}
 
 
 # ------------------------------------------------------------------ workload
