@@ -52,6 +52,7 @@ struct Fwd256Smem {
   int b, qt, kt_lo, nk, n_real, skip;
 };
 static_assert(sizeof(Fwd256Smem) + 1024 <= 232448, "shared memory per CTA");
+static_assert(2 * 2 * kChunkB256 >= kTile * kD256 * 2, "out staging fits ring slots 0-1");
 
 // kMerge: merge this K/V chunk's result into the running (out, lse) instead
 // of writing it (log-sum-exp weights, as the merge kernel).
@@ -353,8 +354,10 @@ __global__ void __launch_bounds__(kThreadsF256, 1)
     ok = __all_sync(0xffffffffu, ok);
     // the last tile's PV products complete after every earlier one
     if (ok && !warp_wait(&s.o_done[(nk - 1) & 1], ((nk - 1) >> 1) & 1, &s.abort_flag, vstatus)) ok = false;
+    if (!ok) s.abort_flag = 1;
+    // the four softmax warps take the same path below (it has a barrier)
+    ok = named_bar_and(1, 128, ok);
     if (!ok) {
-      s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     } else {
       tc_fence_after();
@@ -378,30 +381,62 @@ __global__ void __launch_bounds__(kThreadsF256, 1)
           lse_v = mxl + logf(tot);
         }
       }
+      if constexpr (kMerge) {
 #pragma unroll 1
-      for (int c = 0; c < kD256; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c, o);
-        tmem_wait_ld();
-        if (store) {
+        for (int c = 0; c < kD256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(o[8 * e + k]) * inv;
+              if (kMerge && w_old != 0.f) {
+                const uint4 old = o4[c / 8 + e];
+                const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
+                  v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
+                  v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
+                }
+              }
+              o4[c / 8 + e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                         pack_bf16x2(v[6], v[7]));
+            }
+          }
+        }
+      } else {
+        // out (bf16) staged in ring slots 0-1, which no copy or product uses
+        // once the last tile's PV products are done: row r at 512 r bytes,
+        // 16-byte piece c at slot c ^ (r & 7); then one 512-byte row per warp
+        // store instead of 32 scattered 16-byte pieces
+        uint8_t* stg = &s.ring[0][0][0];
+#pragma unroll 1
+        for (int c = 0; c < kD256; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(o[8 * e + k]) * inv;
-            if (kMerge && w_old != 0.f) {
-              const uint4 old = o4[c / 8 + e];
-              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
-                v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
-                v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
-              }
-            }
-            o4[c / 8 + e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                       pack_bf16x2(v[6], v[7]));
+            const int piece = c / 8 + e;
+            *reinterpret_cast<uint4*>(stg + r * (kD256 * 2) + ((piece ^ (r & 7)) << 4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                           pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
           }
+        }
+        named_bar_sync(1, 128);
+        __nv_bfloat16* obase = out + (static_cast<size_t>(b) * g.Hq + h) * g.L * kD256;
+#pragma unroll 4
+        for (int k2 = 0; k2 < 32; ++k2) {
+          const int rr = (warp & 3) * 32 + k2;
+          const int gi = qt * kTile + rr;
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * (kD256 * 2) + ((lane ^ (rr & 7)) << 4));
+          if (gi < g.L) reinterpret_cast<uint4*>(obase + static_cast<size_t>(gi) * kD256)[lane] = w;
         }
       }
       if (store) lse[row] = lse_v;

@@ -17,7 +17,11 @@
 //               from TMEM, applies the mask only on partial tiles, keeps the
 //               running max / sum in fp32, writes P (bf16) over S in TMEM,
 //               rescales O only when the max grows by more than 2^8, and
-//               finally normalises O and writes out / LSE.
+//               finally normalises O and writes out / LSE: out is staged
+//               as bf16 rows in the K ring (free once the head's last PV
+//               product is done) and copied to global memory a whole row
+//               per 16-byte lane group, so each warp store is one
+//               contiguous 512-byte run instead of 32 scattered pieces.
 // The two q tiles of a CTA share every K/V tile (same kv head), so the tensor
 // core works on one while the other's softmax runs.
 // With attention dropout (kDrop), each softmax thread draws its row's keep
@@ -68,6 +72,7 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
   using Smem = FwdSmem<D, NQ, NS>;
   using TM = FwdTmem<D, NQ>;
   constexpr int kChunks = Smem::kChunks;
+  static_assert(sizeof(Smem::k) >= NQ * kTile * D * 2, "out staging fits the K ring");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw so the compiler keeps the shared address space
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -380,8 +385,10 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !warp_wait(&s.o_done[qi], (nk - 1) & 1, &s.abort_flag, vstatus)) ok = false;
+    if (!ok) s.abort_flag = 1;
+    // the warpgroup's four warps take the same path below (it has a barrier)
+    ok = named_bar_and(1 + qi, 128, ok);
     if (!ok) {
-      s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     } else {
       tc_fence_after();
@@ -405,34 +412,70 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
           lse_v = mx + logf(tot);
         }
       }
+      if constexpr (kMerge) {
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(t_o + c, o);
-        tmem_wait_ld();
-        if (store) {
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+          if (store) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float v[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(o[8 * e + k]) * inv;
+              if (kMerge && w_old != 0.f) {
+                const uint4 old = o4[c / 8 + e];
+                const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
+                  v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
+                  v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
+                }
+              }
+              uint4 w;
+              w.x = pack_bf16x2(v[0], v[1]);
+              w.y = pack_bf16x2(v[2], v[3]);
+              w.z = pack_bf16x2(v[4], v[5]);
+              w.w = pack_bf16x2(v[6], v[7]);
+              o4[c / 8 + e] = w;
+            }
+          }
+        }
+      } else {
+        // O (bf16) of this head into the K ring, which every S product of
+        // this CTA has finished reading once this head's last PV is done:
+        // row r at r * 2D bytes, 16-byte piece c at slot c ^ (r & 7)
+        uint8_t* stg = &s.k[0][0][0] + qi * (kTile * D * 2);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(o[8 * e + k]) * inv;
-            if (kMerge && w_old != 0.f) {
-              const uint4 old = o4[c / 8 + e];
-              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&ow[k]);
-                v[2 * k] = fmaf(w_old, __low2float(h2), v[2 * k]);
-                v[2 * k + 1] = fmaf(w_old, __high2float(h2), v[2 * k + 1]);
-              }
-            }
             uint4 w;
-            w.x = pack_bf16x2(v[0], v[1]);
-            w.y = pack_bf16x2(v[2], v[3]);
-            w.z = pack_bf16x2(v[4], v[5]);
-            w.w = pack_bf16x2(v[6], v[7]);
-            o4[c / 8 + e] = w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * e + 0]) * inv, __uint_as_float(o[8 * e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv);
+            const int piece = c / 8 + e;
+            *reinterpret_cast<uint4*>(stg + r * (D * 2) + ((piece ^ (r & 7)) << 4)) = w;
           }
+        }
+        named_bar_sync(1 + qi, 128);
+        // whole rows to global memory: a warp instruction writes 512
+        // contiguous bytes (2 rows at D = 128, 4 at D = 64)
+        constexpr int kPieces = D / 8, kRows = 32 / kPieces;
+        const int pc = lane % kPieces;
+        __nv_bfloat16* obase = out + (static_cast<size_t>(b) * g.Hq + h) * g.L * D;
+#pragma unroll 4
+        for (int k2 = 0; k2 < 32 / kRows; ++k2) {
+          const int rr = (warp & 3) * 32 + k2 * kRows + lane / kPieces;
+          const int gi = qt * kTile + rr;
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * (D * 2) + ((pc ^ (rr & 7)) << 4));
+          if (gi < g.L) reinterpret_cast<uint4*>(obase + static_cast<size_t>(gi) * D)[pc] = w;
         }
       }
       if (store) lse[row] = lse_v;
