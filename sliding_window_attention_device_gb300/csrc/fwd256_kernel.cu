@@ -102,6 +102,23 @@ __global__ void __launch_bounds__(kThreadsF256, 1)
     }
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
+    if (!s.skip && nk > 0) {
+      // the first copies go out now, ahead of the block barriers and the
+      // tensor-memory allocation: Q, then the halves of K(0) and K(1) into
+      // ring slots 0-3 (units 0-3 of the producer's order)
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&s.q_full, kQChunks256 * kChunkB256);
+      for (int c = 0; c < kQChunks256; ++c) tma_load_3d(s.q[c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h);
+      const int pl = b * g.Hkv + hk;
+      for (int x = 0; x < (nk < 2 ? 2 : 4); ++x) {
+        const int row = (kt_lo + (x >> 1)) * kTile, half = x & 1;
+        mbar_arrive_expect_tx(&s.full[x], 2 * kChunkB256);
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(s.ring[x][c], &tm_k, &s.full[x], (2 * half + c) * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
+      }
+    }
   }
   __syncthreads();
   if (s.skip) return;
@@ -133,13 +150,9 @@ __global__ void __launch_bounds__(kThreadsF256, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    mbar_arrive_expect_tx(&s.q_full, kQChunks256 * kChunkB256);
-    for (int c = 0; c < kQChunks256; ++c) tma_load_3d(s.q[c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h);
+    // (Q and the halves of K(0), K(1) were issued with the barrier set-up)
     const int pl = b * g.Hkv + hk;
-    int u = 0;  // ring units issued
+    int u = nk < 2 ? 2 : 4;  // ring units issued
     // one half of tile t of K or V into the next slot
     auto load_half = [&](const CUtensorMap* map, int t, int half) {
       const int slot = u % kSlots256;
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kThreadsF256, 1)
       return true;
     };
     auto load_tile = [&](const CUtensorMap* map, int t) { return load_half(map, t, 0) && load_half(map, t, 1); };
-    bool ok = load_tile(&tm_k, 0) && (nk < 2 || load_tile(&tm_k, 1));
+    bool ok = true;
     for (int t = 0; ok && t < nk; ++t) ok = load_tile(&tm_v, t) && (t + 2 >= nk || load_tile(&tm_k, t + 2));
     if (!ok) {
       s.abort_flag = 1;

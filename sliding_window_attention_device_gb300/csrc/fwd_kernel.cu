@@ -117,6 +117,27 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
     mbar_init(&s.q_full, 1);
     mbar_init(&s.mma_drain, 1);
     fence_mbar_init();
+    if (!s.skip && nk > 0) {
+      // the first copies go out now, ahead of the block barriers and the
+      // tensor-memory allocation: Q of the heads and K / V of the first tiles
+      const int h0e = pair * NQ, hke = h0e / g.G;
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&s.q_full, NQ * kChunks * Smem::kChunkBytes);
+      for (int qi = 0; qi < NQ; ++qi)
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(s.q[qi][c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h0e + qi);
+      for (int j = 0; j < NS && j < nk; ++j) {
+        const int row = (kt_lo + j) * kTile, pl = b * g.Hkv + hke;
+        mbar_arrive_expect_tx(&s.k_full[j], kChunks * Smem::kChunkBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(s.k[j][c], &tm_k, &s.k_full[j], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
+        mbar_arrive_expect_tx(&s.v_full[j], kChunks * Smem::kChunkBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(s.v[j][c], &tm_v, &s.v_full[j], c * 64, g.kv_tm ? pl : row, g.kv_tm ? row : pl);
+      }
+    }
   }
   __syncthreads();
   if (s.skip) return;
@@ -152,15 +173,9 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    mbar_arrive_expect_tx(&s.q_full, NQ * kChunks * Smem::kChunkBytes);
-    for (int qi = 0; qi < NQ; ++qi)
-      for (int c = 0; c < kChunks; ++c)
-        tma_load_3d(s.q[qi][c], &tm_q, &s.q_full, c * 64, qt * kTile, b * g.Hq + h0 + qi);
-    int k_issued = 0, v_issued = 0;
-    for (int j = 0; j < nk; ++j) {
+    // (Q and the first NS tiles were issued with the barrier set-up)
+    int k_issued = nk < NS ? nk : NS, v_issued = k_issued;
+    for (int j = k_issued; j < nk; ++j) {
       const int st = j % NS, n = j / NS;
       if (j >= NS && !pipe_wait(&s.k_empty[st], (n - 1) & 1, &s.abort_flag, vstatus))
         break;
