@@ -59,7 +59,7 @@ BWD_KERNEL = {64: "bwd128_kernel<64>", 128: "bwd128_kernel<128>", 256: "bwd_kern
               512: "bwd512_kernel (four CTAs per K/V tile, one per 128-column slice)"}
 # the fixed-order dq pass of each head dim above 128
 DQ_KERNEL = {256: "bwd_dq256_kernel", 512: "bwd_dq512_kernel (two CTAs per q tile, one per 256-column half)"}
-TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "d43094137af5baa5", "bytes_per_launch": 1.19089e9}
+TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "8c6ec150f4ea3b55", "bytes_per_launch": 1.63014e9}
 
 
 # ------------------------------------------------------------------ workload
@@ -253,11 +253,12 @@ class Replica:
             self.shards.append(d)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
         # per shard: segment build + classification, forward, backward prep,
-        # zero-fill of unattended dK / dV + backward main, and (bf16 gradients
-        # only) the dq finalize; fp32 dq is accumulated in place
-        self.launches_per_step = (6 if grad_dtype == torch.float32 else 7) * len(self.shards)
-        if deterministic:  # delta, zero-fill, dK / dV, dq: one more launch per shard than the fp32 path
-            self.launches_per_step = 7 * len(self.shards)
+        # backward main (which also writes the zero dK / dV of unattended
+        # tiles), and (bf16 gradients only) the dq finalize; fp32 dq is
+        # accumulated in place
+        self.launches_per_step = (5 if grad_dtype == torch.float32 else 6) * len(self.shards)
+        if deterministic:  # delta, dK / dV, dq: one more launch per shard than the fp32 path
+            self.launches_per_step = 6 * len(self.shards)
         if fwd_only:  # segment build, classification, forward
             self.launches_per_step = 3 * len(self.shards)
 
@@ -350,10 +351,10 @@ class RingChunkReplica(Replica):
                 raise ValueError(f"shard r={sh['r']}: no K/V chunk")
             s["chunks"] = chunks
             n = len(chunks)
-            # per chunk: table build + classification, forward, zero-fill + backward
-            # main; per merge one launch unless fused; per shard the backward prep
+            # per chunk: table build + classification, forward, backward main;
+            # per merge one launch unless fused; per shard the backward prep
             # (and the dq finalize for bf16 gradients)
-            self.launches_per_step += (5 * n + (0 if fused else n - 1) + 1 +
+            self.launches_per_step += (4 * n + (0 if fused else n - 1) + 1 +
                                        (0 if grad_dtype == torch.float32 else 1))
         self.n_merges = sum(len(s["chunks"]) - 1 for s in self.shards)
         self.kv_chunk_bytes = sum(k.numel() * 2 + v.numel() * 2 for k, v in kv_cache.values())
@@ -672,10 +673,10 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "tokens_per_s": round(world * w.B * w.L * len(rep.shards) / (ms_per_step * 1e-3), 1),
         "fwd_tflops": round(fwd_flop * args.steps / (fwd_kernel_ms * 1e-3) / 1e12, 2),
         "bwd_main_tflops": round(bwd_achieved, 2),
-        "roofline": {"kernel": (f"backward: delta, zero-fill, {BWD_KERNEL[w.D]} without dq, "
+        "roofline": {"kernel": (f"backward: delta, {BWD_KERNEL[w.D]} without dq, "
                                 f"{DQ_KERNEL.get(w.D, f'bwd_dq_kernel<{w.D}>')}"
                                 if getattr(rep, "deterministic", False) else
-                                f"{BWD_KERNEL[w.D]} (backward main stage, with its dK/dV zero-fill launch)"),
+                                f"{BWD_KERNEL[w.D]} (backward main stage, zero dK/dV of unattended tiles included)"),
                      "bound": "tensor", "achieved": round(bwd_achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_achieved / peak, 4),
                      **fracs(bwd_achieved), "peak_source": peak_source,

@@ -237,7 +237,7 @@ int bd_attn_bwd(const void* dout, const void* q, const void* k, const void* v, c
  * delta); any head dim (at D = 256 the dq pass streams each K/V tile's K
  * twice, for S and for dQ; at D = 512 two CTAs per q tile and query head each
  * form S and dP for one 256-column half of dq). Three launches: delta,
- * zero-fill + dK / dV, dq. */
+ * dK / dV (with the zero rows of unattended K/V tiles), dq. */
 int bd_attn_bwd_deterministic(const void* dout, const void* q, const void* k, const void* v, const void* out,
                               const float* lse, const void* seg, const bd_geom* g, int grad_dtype, void* dq,
                               void* dk, void* dv, void* workspace, int32_t* status, bd_stream_t stream);

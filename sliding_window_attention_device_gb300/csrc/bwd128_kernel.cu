@@ -36,6 +36,7 @@ namespace {
 constexpr int kQ = 128;          // q rows per tile
 constexpr int kThreads = 512;
 constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
+constexpr int kZeroCtas = 304;  // CTAs that carry the zero-fill (two per SM)
 
 template <int D>
 struct Tiles {
@@ -57,11 +58,11 @@ struct Ctl {
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full, dq_empty, acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int b, kt, q_lo, nq, n_real, skip, mode;
+  int b, kt, q_lo, nq, n_real, skip, mode, n_att;
 };
 
 // What a CTA does, from its position in the backward work list.
-constexpr int kModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
+constexpr int kModeIdle = 0;  // past the attended tiles (their dK / dV zeroed by the working CTAs)
 constexpr int kModeWork = 1;  // an attended K/V tile
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
@@ -111,14 +112,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the attended K/V tiles lead the work list; the grid must cover them
     const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
     int mode = kModeIdle;
-    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv)
+    s.n_att = -1;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv) {
       atomicOr(status, BD_STATUS_BOUNDS);
-    else
+    } else {
       mode = item < n_att ? kModeWork : kModeIdle;
+      s.n_att = n_att;
+    }
     s.mode = mode;
   }
   __syncthreads();
-  if (s.mode != kModeWork) return;
+  // dK / dV of the tiles no local row attends are zero: with attended tiles,
+  // warps 2-3 of the first kZeroCtas working CTAs write them during their main
+  // loop (their tiles come first in the longest-first list, so these CTAs run
+  // longest); with none, the B CTAs per kv head of the grid do it
+  const int n_att_s = s.n_att;
+  if (s.mode != kModeWork) {
+    if (n_att_s == 0)
+      zero_unattended_kv(seg, g, 0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), tid, kThreads, dk, dv,
+                         grads_bf16, status);
+    return;
+  }
 
   if (tid == 0) {
     const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
@@ -488,6 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
+  } else if (warp == 2 || warp == 3) {
+    const int n_w = min(n_att_s * g.Hkv, kZeroCtas);
+    if (static_cast<int>(blockIdx.x) < n_w)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_w, tid - 64, 64, dk, dv, grads_bf16, status);
   } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index == TMEM lane

@@ -47,6 +47,7 @@ constexpr int kStreamed = kD5 / 64 - 2;   // 64-column chunks through the ring p
 constexpr int kKChunkB = kTile * 128;     // 128 rows x 128 B
 constexpr int kQChunkB = kBwdQ * 128;     // 64 rows x 128 B
 constexpr int kThreads5 = 512;
+constexpr int kZeroCtas5 = 304;  // CTAs that carry the zero-fill (two per SM)
 constexpr uint32_t kColS = 0, kColDp = 64, kColDq = 128, kColDv = 256, kColDk = 384;
 
 struct RingSlot {  // chunk e of K, V (the K/V tile's rows) and of Q, dO (the q tile's rows)
@@ -69,7 +70,7 @@ struct Bwd512Smem {
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int b, kt, q64_lo, nq64, n_real, skip, work;
+  int b, kt, q64_lo, nq64, n_real, skip, work, n_att;
 };
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
@@ -101,14 +102,27 @@ __global__ void __launch_bounds__(kThreads5, 1)
     // the attended K/V tiles lead the work list; the grid must cover them
     const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
     int work = 0;
-    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / (kNSlice * g.Hkv))
+    s.n_att = -1;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / (kNSlice * g.Hkv)) {
       atomicOr(status, BD_STATUS_BOUNDS);
-    else
+    } else {
       work = item < n_att ? 1 : 0;
+      s.n_att = n_att;
+    }
     s.work = work;
   }
   __syncthreads();
-  if (!s.work) return;  // past the attended tiles: zeroed by the zero-fill kernel
+  // dK / dV of the tiles no local row attends are zero: with attended tiles,
+  // warps 2-3 of the first kZeroCtas5 working CTAs write them during their
+  // main loop (their tiles come first in the longest-first list, so these CTAs
+  // run longest); with none, the CTAs of the grid do it
+  const int n_att_s = s.n_att;
+  if (!s.work) {
+    if (n_att_s == 0)
+      zero_unattended_kv(seg, g, 0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), tid, kThreads5, dk, dv,
+                         grads_bf16, status);
+    return;
+  }
 
   if (tid == 0) {
     const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
@@ -520,6 +534,10 @@ __global__ void __launch_bounds__(kThreads5, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
+  } else if (warp == 2 || warp == 3) {
+    const int n_w = min(n_att_s * g.Hkv * kNSlice, kZeroCtas5);
+    if (static_cast<int>(blockIdx.x) < n_w)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_w, tid - 64, 64, dk, dv, grads_bf16, status);
   } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the slice == TMEM lane

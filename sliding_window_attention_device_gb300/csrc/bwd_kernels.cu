@@ -159,12 +159,13 @@ struct BwdSmem {
   uint64_t s_full, dp_full, p_full, ds_full, ds_empty, dq_full[2], dq_empty[2], acc_full, acc_empty, mma_drain;
   uint32_t tmem_base;
   int abort_flag;
-  int b, kt, q64_lo, nq64, n_real, skip, mode;
+  int b, kt, q64_lo, nq64, n_real, skip, mode, n_att;
 };
 
 constexpr int kBwdThreads = 512;
+constexpr int kZeroCtasBwd = 304;  // CTAs that carry the zero-fill (two per SM)
 // What a backward CTA does, from its position in the work list.
-constexpr int kBwdModeIdle = 0;  // past the attended tiles (zeroed by the zero-fill kernel)
+constexpr int kBwdModeIdle = 0;  // past the attended tiles (their dK / dV zeroed by the working CTAs)
 constexpr int kBwdModeWork = 1;  // an attended K/V tile
 
 // kDq: with the dq products (else dK / dV only, for the fixed-order dq pass).
@@ -194,14 +195,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the attended K/V tiles lead the work list; the grid must cover them
     const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
     int mode = kBwdModeIdle;
-    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv)
+    s.n_att = -1;
+    if (n_att < 0 || n_att > g.B * g.nkt || n_att > static_cast<int>(gridDim.x) / g.Hkv) {
       atomicOr(status, BD_STATUS_BOUNDS);
-    else
+    } else {
       mode = item < n_att ? kBwdModeWork : kBwdModeIdle;
+      s.n_att = n_att;
+    }
     s.mode = mode;
   }
   __syncthreads();
-  if (s.mode != kBwdModeWork) return;
+  // dK / dV of the tiles no local row attends are zero: with attended tiles,
+  // warps 2-3 of the first kZeroCtasBwd working CTAs write them during their
+  // main loop (their tiles come first in the longest-first list, so these CTAs
+  // run longest); with none, the B CTAs per kv head of the grid do it
+  const int n_att_s = s.n_att;
+  if (s.mode != kBwdModeWork) {
+    if (n_att_s == 0)
+      zero_unattended_kv(seg, g, 0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), tid, kBwdThreads, dk,
+                         dv, grads_bf16, status);
+    return;
+  }
 
   if (tid == 0) {
     const int wi = seg[g.off[BD_SEG_OFF_BWD_WORK] + item];
@@ -597,6 +611,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       s.abort_flag = 1;
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
+  } else if (warp == 2 || warp == 3) {
+    const int n_w = min(n_att_s * g.Hkv, kZeroCtasBwd);
+    if (static_cast<int>(blockIdx.x) < n_w)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_w, tid - 64, 64, dk, dv, grads_bf16, status);
   } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the pass == TMEM lane
@@ -680,21 +698,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// dK / dV of the K/V tiles no local row attends are zero; the attention
-// kernels' CTAs for those tiles exit at once and this streaming kernel writes
-// the zeros (every (tile, kv head) pair past the attended ones in the work list).
-__global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const int32_t* __restrict__ seg, const Geom g, void* dk,
-                                                          void* dv, int grads_bf16, int32_t* status) {
-  pdl_begin();
-  const int n_att = seg[g.off[BD_SEG_OFF_COUNTS] + 3];
-  if (n_att < 0 || n_att > g.B * g.nkt) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, BD_STATUS_BOUNDS);
-    return;
-  }
-  zero_unattended_kv(seg, g, n_att, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                     static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x), dk, dv, grads_bf16, status);
-}
 
 unsigned grid_for(long long work_items) {
   const long long blocks = (work_items + 255) / 256;
@@ -796,14 +799,6 @@ cudaError_t launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mdo, const
                             void* dv, int bf16, void* workspace, float* dq_f32, int32_t* status, cudaStream_t st) {
   float* dq_acc = dq_f32 ? dq_f32 : static_cast<float*>(workspace);
   const float* delta = ws_delta(g, workspace);
-  {
-    const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
-    const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
-    if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
-        status); le != cudaSuccess) return le;
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   switch (g.D) {
     case 64:
     case 128:  // 128-row q tiles (bwd128_kernel.cu); q / dout maps use 128-row boxes
@@ -823,10 +818,6 @@ cudaError_t launch_bwd_main_nodq(const CUtensorMap& mq, const CUtensorMap& mdo, 
                                  const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,
                                  void* dk, void* dv, int bf16, void* workspace, int32_t* status, cudaStream_t st) {
   if (g.D != 64 && g.D != 128 && g.D != 256 && g.D != 512) return cudaErrorInvalidValue;
-  const long long pairs = static_cast<long long>(g.B) * g.nkt * g.Hkv;  // upper bound on zero tiles
-  const unsigned grid = static_cast<unsigned>(pairs < 152 * 8 ? (pairs > 0 ? pairs : 1) : 152 * 8);
-  if (const cudaError_t le = launch_pdl(bwd_zero_kv_kernel, dim3(grid), dim3(256), 0, st, seg, g, dk, dv, bf16,
-      status); le != cudaSuccess) return le;
   if (g.D == 512)
     return launch_bwd512_main(mq, mdo, mk, mv, seg, g, lse, ws_delta(g, workspace), nullptr, dk, dv, bf16, status,
                               st);
