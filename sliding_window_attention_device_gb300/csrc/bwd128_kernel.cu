@@ -36,7 +36,7 @@ namespace {
 constexpr int kQ = 128;          // q rows per tile
 constexpr int kThreads = 512;
 constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
-constexpr int kZeroCtas = 304;  // CTAs that carry the zero-fill (two per SM)
+constexpr int kZeroCtas = 152;  // CTAs that carry the zero-fill (the first wave on 152 SMs)
 
 template <int D>
 struct Tiles {

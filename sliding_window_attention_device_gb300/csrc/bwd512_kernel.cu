@@ -47,7 +47,7 @@ constexpr int kStreamed = kD5 / 64 - 2;   // 64-column chunks through the ring p
 constexpr int kKChunkB = kTile * 128;     // 128 rows x 128 B
 constexpr int kQChunkB = kBwdQ * 128;     // 64 rows x 128 B
 constexpr int kThreads5 = 512;
-constexpr int kZeroCtas5 = 304;  // CTAs that carry the zero-fill (two per SM)
+constexpr int kZeroCtas5 = 152;  // CTAs that carry the zero-fill (the first wave on 152 SMs)
 constexpr uint32_t kColS = 0, kColDp = 64, kColDq = 128, kColDv = 256, kColDk = 384;
 
 struct RingSlot {  // chunk e of K, V (the K/V tile's rows) and of Q, dO (the q tile's rows)

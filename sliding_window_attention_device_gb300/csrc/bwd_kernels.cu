@@ -163,7 +163,7 @@ struct BwdSmem {
 };
 
 constexpr int kBwdThreads = 512;
-constexpr int kZeroCtasBwd = 304;  // CTAs that carry the zero-fill (two per SM)
+constexpr int kZeroCtasBwd = 152;  // CTAs that carry the zero-fill (the first wave on 152 SMs)
 // What a backward CTA does, from its position in the work list.
 constexpr int kBwdModeIdle = 0;  // past the attended tiles (their dK / dV zeroed by the working CTAs)
 constexpr int kBwdModeWork = 1;  // an attended K/V tile
