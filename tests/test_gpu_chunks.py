@@ -32,6 +32,8 @@ CASES = [
                      layout=("uniform", 50, 400, 70), window=100), 1, (0, 128, 517, None)),
     ("d256_window", W("cc", "chunked, D 256, window 150", B=1, Hq=4, Hkv=2, D=256, S=1280, cp_size=4,
                       layout=("uniform", 100, 600, 30), window=150, kv="prefix"), 3, (0, 830, 1000, None)),
+    ("d256_after", W("ce", "chunked, D 256, GQA 2, a chunk after the rows", B=2, Hq=4, Hkv=2, D=256, S=1024,
+                     cp_size=4, layout=("uniform", 60, 500, 20), kv="prefix"), 1, (0, 200, None)),
     ("d512_prefix", W("cd", "chunked, D 512, GQA 2", B=1, Hq=4, Hkv=2, D=512, S=1024, cp_size=4,
                       layout=("uniform", 60, 500, 20), kv="prefix"), 2, (0, 300, 700, None)),
 ]
