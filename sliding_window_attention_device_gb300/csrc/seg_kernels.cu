@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restri
 
   // Layout over the whole row: ids >= 0, no document after padding.
   int bad = 0;
+#pragma unroll 8
   for (int p = tid; p < g.S_full; p += nthr) {
     const int c = row[p];
     if (c < 0 || (p > 0 && c != 0 && row[p - 1] == 0)) bad = 1;
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(1024) seg_build_kernel(const int32_t* __restri
   // the straddle. Otherwise check every segment exactly.
   if (n_seg > 0) {
     int m0 = INT_MIN;
+#pragma unroll 8
     for (int p = tid; p < s_first; p += nthr) m0 = max(m0, row[p]);
     m0 = block_reduce(m0, MaxOp(), s_red);
     int fast_ok = 1;
