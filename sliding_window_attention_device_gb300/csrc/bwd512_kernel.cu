@@ -112,15 +112,17 @@ __global__ void __launch_bounds__(kThreads5, 1)
     s.work = work;
   }
   __syncthreads();
-  // dK / dV of the tiles no local row attends are zero: with attended tiles,
-  // warps 2-3 of the first kZeroCtas5 working CTAs write them during their
-  // main loop (their tiles come first in the longest-first list, so these CTAs
-  // run longest); with none, the CTAs of the grid do it
+  // dK / dV of the tiles no local row attends are zero. With at least a wave
+  // of working CTAs, warps 2-3 of the first kZeroCtas5 of them write these
+  // rows during their main loop (their tiles lead the longest-first list, so
+  // these CTAs run longest); with fewer, every CTA of the grid takes a share,
+  // the idle ones with all their threads.
   const int n_att_s = s.n_att;
+  const int n_zw = n_att_s * g.Hkv * kNSlice >= kZeroCtas5 ? kZeroCtas5 : static_cast<int>(gridDim.x);
   if (!s.work) {
-    if (n_att_s == 0)
-      zero_unattended_kv(seg, g, 0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), tid, kThreads5, dk, dv,
-                         grads_bf16, status);
+    if (n_att_s >= 0 && static_cast<int>(blockIdx.x) < n_zw)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_zw, tid, kThreads5, dk, dv, grads_bf16,
+                         status);
     return;
   }
 
@@ -535,9 +537,8 @@ __global__ void __launch_bounds__(kThreads5, 1)
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
   } else if (warp == 2 || warp == 3) {
-    const int n_w = min(n_att_s * g.Hkv * kNSlice, kZeroCtas5);
-    if (static_cast<int>(blockIdx.x) < n_w)
-      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_w, tid - 64, 64, dk, dv, grads_bf16, status);
+    if (static_cast<int>(blockIdx.x) < n_zw)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_zw, tid - 64, 64, dk, dv, grads_bf16, status);
   } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the slice == TMEM lane
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(kThreads5, 1)
 
 // K4e launch: one CTA per (attended K/V tile, kv head, 128-column slice), the
 // four slices of a tile adjacent in the grid; only tiles some local row can
-// reach by position get CTAs (the zero-fill kernel writes the others' zeros).
+// reach by position get working CTAs (the first of them also write the others' zeros).
 // Without a dq accumulator (dq_acc null) the dq products are left out.
 cudaError_t launch_bwd512_main(const CUtensorMap& mq, const CUtensorMap& mdo, const CUtensorMap& mk,
                                const CUtensorMap& mv, const int32_t* seg, const Geom& g, const float* lse,

@@ -205,15 +205,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     s.mode = mode;
   }
   __syncthreads();
-  // dK / dV of the tiles no local row attends are zero: with attended tiles,
-  // warps 2-3 of the first kZeroCtasBwd working CTAs write them during their
-  // main loop (their tiles come first in the longest-first list, so these CTAs
-  // run longest); with none, the B CTAs per kv head of the grid do it
+  // dK / dV of the tiles no local row attends are zero. With at least a wave
+  // of working CTAs, warps 2-3 of the first kZeroCtasBwd of them write these
+  // rows during their main loop (their tiles lead the longest-first list, so
+  // these CTAs run longest); with fewer, every CTA of the grid takes a share,
+  // the idle ones with all their threads.
   const int n_att_s = s.n_att;
+  const int n_zw = n_att_s * g.Hkv >= kZeroCtasBwd ? kZeroCtasBwd : static_cast<int>(gridDim.x);
   if (s.mode != kBwdModeWork) {
-    if (n_att_s == 0)
-      zero_unattended_kv(seg, g, 0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), tid, kBwdThreads, dk,
-                         dv, grads_bf16, status);
+    if (n_att_s >= 0 && static_cast<int>(blockIdx.x) < n_zw)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_zw, tid, kBwdThreads, dk, dv, grads_bf16,
+                         status);
     return;
   }
 
@@ -612,9 +614,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) atomicOr(status, BD_STATUS_TIMEOUT);
     }
   } else if (warp == 2 || warp == 3) {
-    const int n_w = min(n_att_s * g.Hkv, kZeroCtasBwd);
-    if (static_cast<int>(blockIdx.x) < n_w)
-      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_w, tid - 64, 64, dk, dv, grads_bf16, status);
+    if (static_cast<int>(blockIdx.x) < n_zw)
+      zero_unattended_kv(seg, g, n_att_s, static_cast<int>(blockIdx.x), n_zw, tid - 64, 64, dk, dv, grads_bf16, status);
   } else if (kDq && warp >= 8 && warp < 12) {
     // ----------------------------------------------- dQ read-out (d rows)
     const int r = tid - 256;  // d index within the pass == TMEM lane
