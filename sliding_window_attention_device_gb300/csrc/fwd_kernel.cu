@@ -463,11 +463,14 @@ __global__ void __launch_bounds__(128 + NQ * 128, 1)
         // this CTA has finished reading once this head's last PV is done:
         // row r at r * 2D bytes, 16-byte piece c at slot c ^ (r & 7)
         uint8_t* stg = &s.k[0][0][0] + qi * (kTile * D * 2);
-#pragma unroll 1
+        uint32_t oa[D];  // all of O's row, one wait
+#pragma unroll
+        for (int c = 0; c < D; c += 32) tmem_ld32(t_o + c, *reinterpret_cast<uint32_t(*)[32]>(&oa[c]));
+        tmem_wait_ld();
+        tmem_regs_ready<D>(oa);
+#pragma unroll
         for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(t_o + c, o);
-          tmem_wait_ld();
+          const uint32_t* o = oa + c;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 w;
