@@ -59,7 +59,7 @@ BWD_KERNEL = {64: "bwd128_kernel<64>", 128: "bwd128_kernel<128>", 256: "bwd_kern
               512: "bwd512_kernel (four CTAs per K/V tile, one per 128-column slice)"}
 # the fixed-order dq pass of each head dim above 128
 DQ_KERNEL = {256: "bwd_dq256_kernel", 512: "bwd_dq512_kernel (two CTAs per q tile, one per 256-column half)"}
-TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "b8555b03c0349452", "bytes_per_launch": 1.60618e9}
+TRAFFIC = {"kernel": "bwd128_kernel<128>", "workload": "C2", "source_sha256": "197ab565abf9f318", "bytes_per_launch": 1.60883e9}
 
 
 # ------------------------------------------------------------------ workload
