@@ -36,6 +36,9 @@ CASES = [
     ("d512_len1_docs", W("l", 1, 2, 1, 512, 640, 2, ("uniform", 1, 3, 17)), (0,)),
     ("d512_window1", W("m", 1, 2, 1, 512, 512, 2, ("uniform", 30, 200, 5), window=1), (1,)),
     ("d512_all_pad_shard", W("n", 1, 2, 1, 512, 1024, 4, ("explicit", (300, 200), 524)), (2, 3)),
+    ("d256_len1_docs", W("o", 1, 2, 1, 256, 640, 2, ("uniform", 1, 3, 17)), (0,)),
+    ("d256_window1", W("p", 1, 2, 1, 256, 512, 2, ("uniform", 30, 200, 5), window=1), (1,)),
+    ("d256_all_pad_shard", W("q", 1, 2, 1, 256, 1024, 4, ("explicit", (300, 200), 524)), (2, 3)),
 ]
 
 
