@@ -52,3 +52,11 @@ def test_peak_follows_the_clock_record():
                    {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}):
         p, src = bench.choose_peak(peaks, clocks)
         assert p == 1686.5 and "sustained" in src, clocks
+
+
+def test_end_to_end_bound():
+    """The end-to-end bound is the slowest of the device step and the two copy
+    directions at their measured rates (C2: 5.9 GB out at 193 GB/s)."""
+    assert bench.e2e_bound_ms(9.75, 1.342e9, 5.914e9, 210.0, 193.0) == pytest.approx(30.64, abs=0.01)
+    assert bench.e2e_bound_ms(50.0, 1e9, 1e9, 200.0, 200.0) == 50.0  # device-bound
+    assert bench.e2e_bound_ms(1.0, 4e9, 1e9, 200.0, 200.0) == pytest.approx(20.0)  # host-to-device-bound
