@@ -35,7 +35,7 @@ DEEP = {
 
 # (workload, rank, kv groups)
 SUBSETS = [("C2", 0, (0, 7)), ("C2", 4, (0, 7)), ("C2", 7, (0, 7)), ("C3", 7, (0, 7)), ("C5", 3, (0,)),
-           ("C5w512", 3, (0,)), ("deep16k", 7, (0,))]
+           ("C5w512", 3, (0,)), ("deep16k", 7, (0,)), ("G512", 5, (0,))]
 
 
 def _workload(key):
